@@ -1,0 +1,392 @@
+"""Seeded synthetic workloads for the token-tree verification step.
+
+This module only makes inputs: candidate trees (parent lists), draft and
+target token ids, bf16 Q/K/V drawn from N(0, 1), prompt lengths and a paged KV
+pool with a shuffled block table. It holds none of the step's arithmetic (no
+masks, RoPE, attention, acceptance or commit), so both the CUDA path and the
+CPU oracle can be fed from it.
+
+Tree shapes follow the proposal methods the pages describe:
+  * Medusa cartesian trees - "02 · Token Tree 与 Tree Attention", §3: head k
+    contributes its top-s_k tokens under every depth-(k-1) node.
+  * EAGLE-2 dynamic trees - same page §3 and §5: each layer expands the top-k
+    nodes of the previous layer by cumulative (prefix survival) log-probability
+    and the global top-N nodes are kept.
+  * DDTree trees - "Accelerating Speculative Decoding with Block Diffusion
+    Draft Trees", §4-§5: factorised per-position marginals, per-depth top-K
+    (Lemma 1) and a best-first heap over rank tuples (Algorithm 1) that pops
+    the B most probable prefixes.
+
+Readings where the workload descriptions are silent: N(0, s) means standard
+deviation s; "the target matches the draft child with probability p" means a
+node with children gets, with probability p, the token of a uniformly chosen
+child as its target id, otherwise a uniform id (leaves always get a uniform
+id); ties in the tree selections go to the shallower node, then the earlier
+generated one.
+"""
+
+from __future__ import annotations
+
+import heapq
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+VOCAB_LLAMA = 32000
+VOCAB_QWEN = 151936
+
+
+def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (torch's round-to-nearest-even) and return
+    the uint16 bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def normal_bf16(rng: np.random.Generator, shape, chunk=1 << 24) -> np.ndarray:
+    """bf16 bit patterns of N(0, 1) draws, generated in chunks to bound memory."""
+    total = int(np.prod(shape))
+    out = np.empty(total, dtype=np.uint16)
+    for s in range(0, total, chunk):
+        e = min(total, s + chunk)
+        out[s:e] = bf16_bits_from_f32(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+# --------------------------------------------------------------------------
+# tree shapes
+
+
+def medusa_tree(rng, sizes, vocab):
+    """Cartesian Medusa tree in BFS order: returns (parents, tokens) without
+    the root's token (node 0 is the root; tokens[0] is filled by the caller)."""
+    parents, tokens = [-1], [0]
+    frontier = [0]
+    for s in sizes:
+        head_tokens = rng.choice(vocab, size=s, replace=False)
+        nxt = []
+        for p in frontier:
+            for t in head_tokens:
+                parents.append(p)
+                tokens.append(int(t))
+                nxt.append(len(parents) - 1)
+        frontier = nxt
+    return np.array(parents, np.int32), np.array(tokens, np.int32)
+
+
+def _topk_logprobs(rng, vocab, k, sigma):
+    logits = rng.standard_normal(vocab) * sigma
+    m = logits.max()
+    lse = m + math.log(np.exp(logits - m).sum())
+    idx = np.argpartition(-logits, k - 1)[:k]
+    idx = idx[np.lexsort((idx, -logits[idx]))]        # descending, ties by id
+    return idx.astype(np.int64), logits[idx] - lse
+
+
+def eagle_tree(rng, depth, topk, keep, vocab, sigma=2.0, until_count=False,
+               max_layers=32):
+    """EAGLE-2 style dynamic tree.
+
+    Layer 1 is the root's top-k children; layer l expands the top-k nodes of
+    layer l-1 (by cumulative log-prob) with their own top-k children. With
+    ``until_count`` layers are added until at least ``keep`` candidates exist
+    (at most ``max_layers``) instead of exactly ``depth`` layers. The global
+    top-``keep`` candidates by cumulative score are kept (prefix-closed because
+    every child scores strictly below its parent) and packed in BFS order.
+    Returns (parents, tokens, scores) with node 0 the root.
+    """
+    # candidate: (score, depth, gen, parent_gen, rank, token)
+    cands = []
+    toks, lps = _topk_logprobs(rng, vocab, topk, sigma)
+    layer = []
+    for r in range(topk):
+        c = (float(lps[r]), 1, len(cands), -1, r, int(toks[r]))
+        cands.append(c)
+        layer.append(c)
+    n_layers = 1
+    while True:
+        if until_count:
+            if len(cands) >= keep or n_layers >= max_layers:
+                break
+        elif n_layers >= depth:
+            break
+        best = sorted(layer, key=lambda c: (-c[0], c[2]))[:topk]
+        layer = []
+        for pc in best:
+            toks, lps = _topk_logprobs(rng, vocab, topk, sigma)
+            for r in range(topk):
+                c = (pc[0] + float(lps[r]), pc[1] + 1, len(cands), pc[2], r, int(toks[r]))
+                cands.append(c)
+                layer.append(c)
+        n_layers += 1
+    kept = sorted(cands, key=lambda c: (-c[0], c[1], c[2]))[:keep]
+    kept_gen = {c[2] for c in kept}
+    for c in kept:
+        if c[3] != -1 and c[3] not in kept_gen:
+            raise AssertionError("eagle_tree selection is not prefix-closed")
+    # BFS packing: by depth, then parent's packed index, then child rank.
+    packed_of = {-1: 0}
+    order = []
+    for dpt in range(1, max(c[1] for c in kept) + 1):
+        level = [c for c in kept if c[1] == dpt]
+        level.sort(key=lambda c: (packed_of[c[3]], c[4]))
+        for c in level:
+            packed_of[c[2]] = len(order) + 1
+            order.append(c)
+    parents = [-1] + [packed_of[c[3]] for c in order]
+    tokens = [0] + [c[5] for c in order]
+    scores = [0.0] + [c[0] for c in order]
+    return np.array(parents, np.int32), np.array(tokens, np.int32), np.array(scores)
+
+
+def ddtree_marginals(rng, length, vocab, sigma=3.0, k=None):
+    """Per-position drafter marginals softmax(N(0, sigma) logits).
+
+    Returns (top_tokens [L, K], top_logq [L, K]) holding the K most probable
+    tokens per position in descending probability (Lemma 1 of the DDTree notes:
+    only the per-depth top-K tokens, K = min(B, |V|), can appear in an optimal
+    tree)."""
+    k = vocab if k is None else min(k, vocab)
+    toks = np.zeros((length, k), np.int64)
+    logq = np.zeros((length, k))
+    for i in range(length):
+        t, lp = _topk_logprobs(rng, vocab, k, sigma)
+        toks[i], logq[i] = t, lp
+    return toks, logq
+
+
+def ddtree_heap(logq, budget):
+    """Best-first enumeration of the ``budget`` most probable prefixes over
+    rank tuples (Algorithm 1 of the DDTree notes, §5).
+
+    logq [L, K]: per-position log-probabilities sorted descending. Ranks are
+    0-based here. Returns the popped rank tuples in pop order and their scores.
+    Ties pop the shallower tuple first, then the lexicographically smaller one.
+    """
+    length, k = logq.shape
+    heap = [(-logq[0, 0], 1, (0,))]
+    popped, scores = [], []
+    while heap and len(popped) < budget:
+        neg, _, rho = heapq.heappop(heap)
+        score = -neg
+        popped.append(rho)
+        scores.append(score)
+        d = len(rho)
+        last = rho[-1]
+        if last + 1 < k:                               # next sibling
+            sib = rho[:-1] + (last + 1,)
+            s = score - logq[d - 1, last] + logq[d - 1, last + 1]
+            heapq.heappush(heap, (-s, d, sib))
+        if d < length:                                 # first child
+            child = rho + (0,)
+            heapq.heappush(heap, (-(score + logq[d, 0]), d + 1, child))
+    return popped, scores
+
+
+def ddtree_tree(rng, length, vocab, budget, sigma=3.0):
+    """DDTree: (parents, tokens, rank_tuples) with node 0 the root and the
+    popped prefixes packed in pop order (parents always precede children)."""
+    toks, logq = ddtree_marginals(rng, length, vocab, sigma, k=budget)
+    popped, _ = ddtree_heap(logq, budget)
+    index = {(): 0}
+    parents, tokens = [-1], [0]
+    for rho in popped:
+        index[rho] = len(parents)
+        parents.append(index[rho[:-1]])
+        tokens.append(int(toks[len(rho) - 1, rho[-1]]))
+    return np.array(parents, np.int32), np.array(tokens, np.int32), popped
+
+
+def target_ids_for(rng, parents, tokens, vocab, p_match):
+    """Synthetic per-node target (greedy) ids: with probability ``p_match`` a
+    node with children points at a uniformly chosen child's token."""
+    n = len(parents)
+    children = [[] for _ in range(n)]
+    for j in range(1, n):
+        children[int(parents[j])].append(j)
+    tgt = rng.integers(0, vocab, size=n).astype(np.int32)
+    for i in range(n):
+        if children[i] and rng.random() < p_match:
+            tgt[i] = tokens[children[i][int(rng.integers(len(children[i])))]]
+    return tgt
+
+
+# --------------------------------------------------------------------------
+# batches
+
+
+@dataclass
+class Geometry:
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int = 16
+    rope_base: float = 10000.0
+    rope_style: int = 0
+
+
+def assemble(rng, geom: Geometry, prompt_lens, trees, vocab, p_match,
+             max_nodes=None, slack_blocks=None, extra_slots=0, cache_fill="normal"):
+    """Build one batch.
+
+    trees: list of (parents, tokens) per request (node 0 = root). Returns a
+    dict with every array the step consumes (bf16 tensors as uint16 bits).
+    ``extra_slots`` reserves block-table room for later steps.
+    """
+    bsz = len(trees)
+    bs = geom.block_size
+    counts = [len(t[0]) for t in trees]
+    cu = np.zeros(bsz + 1, np.int32)
+    cu[1:] = np.cumsum(counts)
+    total = int(cu[-1])
+    if max_nodes is None:
+        max_nodes = max(counts)
+    parents = np.concatenate([t[0] for t in trees]).astype(np.int32)
+    tokens = np.concatenate([t[1] for t in trees]).astype(np.int32)
+    # the root's token is the previous round's bonus token
+    for b in range(bsz):
+        tokens[cu[b]] = int(rng.integers(0, vocab))
+    targets = np.concatenate([
+        target_ids_for(rng, trees[b][0], tokens[cu[b]:cu[b + 1]], vocab, p_match)
+        for b in range(bsz)]).astype(np.int32)
+    plen = np.asarray(prompt_lens, np.int32)
+    need = [-(-(int(plen[b]) + counts[b]) // bs) for b in range(bsz)]
+    max_blocks = max(-(-(int(plen[b]) + counts[b] + extra_slots) // bs) for b in range(bsz))
+    if slack_blocks is None:
+        slack_blocks = max(16, sum(need) // 20)
+    num_blocks = sum(need) + slack_blocks + bsz * max(0, max_blocks - max(need))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    table = np.full((bsz, max_blocks), -1, np.int32)
+    used = 0
+    for b in range(bsz):
+        table[b, :need[b]] = perm[used:used + need[b]]
+        used += need[b]
+    free = [int(x) for x in perm[used:]]
+    hq, hkv, d = geom.num_q_heads, geom.num_kv_heads, geom.head_dim
+    pool_shape = (num_blocks, hkv, bs, d)
+    if cache_fill == "normal":
+        k_cache = normal_bf16(rng, pool_shape)
+        v_cache = normal_bf16(rng, pool_shape)
+    else:
+        k_cache = np.zeros(pool_shape, np.uint16)
+        v_cache = np.zeros(pool_shape, np.uint16)
+    return {
+        "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "block_size": bs,
+        "rope_base": geom.rope_base, "rope_style": geom.rope_style,
+        "batch": bsz, "max_nodes": int(max_nodes), "max_depth": int(max_nodes) - 1,
+        "vocab": vocab, "cu_nodes": cu, "parents": parents, "prompt_len": plen,
+        "draft_tokens": tokens, "target_ids": targets,
+        "q": normal_bf16(rng, (total, hq, d)),
+        "k_new": normal_bf16(rng, (total, hkv, d)),
+        "v_new": normal_bf16(rng, (total, hkv, d)),
+        "block_table": table, "n_blocks": np.array(need, np.int32),
+        "max_blocks_per_req": int(max_blocks), "num_blocks": int(num_blocks),
+        "k_cache": k_cache, "v_cache": v_cache, "free_blocks": free,
+        "p_match": p_match,
+    }
+
+
+CONFIG_NAMES = {
+    1: "tiny: B=1 Hq4/Hkv2/D64 P=7 Medusa 2x3 (9 nodes)",
+    2: "llama3-8b-attn B=8 P~U[512,2048] Medusa 4x3x2 (41 nodes)",
+    3: "llama3-8b-attn B=32 P~U[1024,8192] EAGLE-2 d6 k8 top-64 (65 nodes)",
+    4: "llama3-70b-attn B=16 P~U[2048,4096] DDTree L16 V151936 B256 (257 nodes)",
+    5: "llama3-8b-attn B=64 ragged P~logU[4096,32768] random EAGLE N in {16..128}",
+}
+
+GEOM_8B = Geometry(32, 8, 128)
+GEOM_70B = Geometry(64, 8, 128)
+GEOM_TINY = Geometry(4, 2, 64)
+
+
+def make_config(idx: int, batch=None, seed=None, prompt_scale=1.0, cache_fill="normal"):
+    """The five verification workloads (seed 1000 + idx by default).
+
+    ``batch`` and ``prompt_scale`` shrink a workload for quick checks (the
+    tree recipe is unchanged)."""
+    rng = np.random.default_rng(1000 + idx if seed is None else seed)
+    if idx == 1:
+        bsz = batch or 1
+        trees = [medusa_tree(rng, (2, 3), VOCAB_LLAMA) for _ in range(bsz)]
+        plens = [7] * bsz
+        return assemble(rng, GEOM_TINY, plens, trees, VOCAB_LLAMA, 0.5,
+                        cache_fill=cache_fill) | {"config": 1}
+    if idx == 2:
+        bsz = batch or 8
+        plens = rng.integers(512, 2049, size=bsz)
+        trees = [medusa_tree(rng, (4, 3, 2), VOCAB_LLAMA) for _ in range(bsz)]
+        geom = GEOM_8B
+    elif idx == 3:
+        bsz = batch or 32
+        plens = rng.integers(1024, 8193, size=bsz)
+        trees = [eagle_tree(rng, 6, 8, 64, VOCAB_LLAMA, 2.0)[:2] for _ in range(bsz)]
+        geom = GEOM_8B
+    elif idx == 4:
+        bsz = batch or 16
+        plens = rng.integers(2048, 4097, size=bsz)
+        trees = [ddtree_tree(rng, 16, VOCAB_QWEN, 256, 3.0)[:2] for _ in range(bsz)]
+        geom = GEOM_70B
+        plens = (np.asarray(plens) * prompt_scale).astype(np.int64)
+        return assemble(rng, geom, plens, trees, VOCAB_QWEN, 0.7,
+                        cache_fill=cache_fill) | {"config": 4}
+    elif idx == 5:
+        bsz = batch or 64
+        plens = np.exp(rng.uniform(math.log(4096), math.log(32768), size=bsz)).astype(np.int64)
+        trees = []
+        for _ in range(bsz):
+            n_tree = int(rng.choice([16, 32, 64, 128]))
+            k = int(rng.integers(4, 11))
+            trees.append(eagle_tree(rng, 0, k, n_tree, VOCAB_LLAMA, 2.0, until_count=True)[:2])
+        plens = (np.asarray(plens) * prompt_scale).astype(np.int64)
+        return assemble(rng, GEOM_8B, plens, trees, VOCAB_LLAMA, 0.6, max_nodes=129,
+                        extra_slots=8 * 130, cache_fill=cache_fill) | {"config": 5}
+    else:
+        raise ValueError(f"unknown config {idx}")
+    plens = (np.asarray(plens) * prompt_scale).astype(np.int64)
+    return assemble(rng, geom, plens, trees, VOCAB_LLAMA, 0.7,
+                    cache_fill=cache_fill) | {"config": idx}
+
+
+def next_step_inputs(rng, w, new_len, bonus, trees, p_match=None):
+    """Inputs of the following verification step of a multi-step run.
+
+    new_len / bonus come from the previous step's commit; ``trees`` are the new
+    candidate trees. The paged pool, block table and free list in ``w`` are the
+    post-commit state; blocks for the new tentative slots are taken from
+    ``w['free_blocks']`` (front first). Returns a new dict (pool arrays shared).
+    """
+    bsz = w["batch"]
+    bs = w["block_size"]
+    vocab = w["vocab"]
+    p_match = w["p_match"] if p_match is None else p_match
+    counts = [len(t[0]) for t in trees]
+    cu = np.zeros(bsz + 1, np.int32)
+    cu[1:] = np.cumsum(counts)
+    total = int(cu[-1])
+    tokens = np.concatenate([t[1] for t in trees]).astype(np.int32)
+    for b in range(bsz):
+        tokens[cu[b]] = int(bonus[b])
+    targets = np.concatenate([
+        target_ids_for(rng, trees[b][0], tokens[cu[b]:cu[b + 1]], vocab, p_match)
+        for b in range(bsz)]).astype(np.int32)
+    table = np.array(w["block_table"], copy=True)
+    n_blocks = np.array(w["n_blocks"], copy=True)
+    free = list(w["free_blocks"])
+    for b in range(bsz):
+        need = -(-(int(new_len[b]) + counts[b]) // bs)
+        if need > table.shape[1]:
+            raise RuntimeError("block table too small for the next step")
+        while n_blocks[b] < need:
+            table[b, n_blocks[b]] = free.pop(0)
+            n_blocks[b] += 1
+    hq, hkv, d = w["num_q_heads"], w["num_kv_heads"], w["head_dim"]
+    out = dict(w)
+    out.update(
+        cu_nodes=cu, parents=np.concatenate([t[0] for t in trees]).astype(np.int32),
+        prompt_len=np.asarray(new_len, np.int32), draft_tokens=tokens, target_ids=targets,
+        q=normal_bf16(rng, (total, hq, d)), k_new=normal_bf16(rng, (total, hkv, d)),
+        v_new=normal_bf16(rng, (total, hkv, d)), block_table=table, n_blocks=n_blocks,
+        free_blocks=free)
+    return out
