@@ -1,0 +1,431 @@
+"""Benchmark of one token-tree verification step on GB300.
+
+A step is the whole hot path over one batch: tv_tree_build ->
+tv_tree_attention_verify -> tv_greedy_accept -> tv_kv_commit (plus the
+block-table refill a serving loop's allocator does before the next step).
+The default workload is the Llama-3-8B attention geometry, batch 8, prompt
+lengths U[512, 2048], Medusa 4x3x2 trees (41 nodes incl. root), paged KV
+block 16 with a shuffled block table.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+Under torchrun every rank runs its own batch (requests are independent: no
+data-path collective); rank 0 prints one JSON line. ``--impl reference`` times
+the CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify tokens/s at 1 GB300; attention HBM GB/s & % roofline per step"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+ATTN_SOURCES = ("attention_mma.cu", "tv_plan.cuh", "tv_common.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(w):
+    plen = np.asarray(w["prompt_len"])
+    cu = np.asarray(w["cu_nodes"])
+    return {
+        "workload": {2: "llama3-8b-attn-medusa", 3: "llama3-8b-attn-eagle2",
+                     4: "llama3-70b-attn-ddtree", 5: "llama3-8b-attn-ragged-eagle",
+                     1: "tiny-medusa"}.get(w["config"], str(w["config"])),
+        "description": __import__("speculative_decoding_tree_build_gb300.workloads",
+                                  fromlist=["CONFIG_NAMES"]).CONFIG_NAMES[w["config"]],
+        "batch": int(w["batch"]), "num_q_heads": w["num_q_heads"],
+        "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+        "block_size": w["block_size"], "tree_nodes_per_request": sorted(set(np.diff(cu).tolist())),
+        "prompt_len_mean": float(plen.mean()), "prompt_len_min": int(plen.min()),
+        "prompt_len_max": int(plen.max()), "seed": 1000 + int(w["config"]),
+        "l2": "flushed between timed steps (512 MiB write)",
+    }
+
+
+def attention_algorithmic(w, depth):
+    """Algorithmic bytes and FLOPs of one tv_tree_attention_verify launch."""
+    hq, hkv, d = w["num_q_heads"], w["num_kv_heads"], w["head_dim"]
+    cu = np.asarray(w["cu_nodes"])
+    nbytes = 0
+    flops = 0
+    for b in range(w["batch"]):
+        n = int(cu[b + 1] - cu[b])
+        p = int(w["prompt_len"][b])
+        nbytes += 2 * hkv * d * 2 * p                # prompt K + V read
+        nbytes += n * (hq + 2 * hkv) * d * 2         # raw q, k, v read
+        nbytes += n * 2 * hkv * d * 2                # rotated K + V written to the cache
+        nbytes += n * hq * d * 2                     # output written
+        flops += 4 * hq * d * n * p
+        flops += 4 * hq * d * int(np.sum(depth[cu[b]:cu[b + 1]] + 1))
+    return nbytes, flops
+
+
+def attn_source_sha():
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current attention source."""
+    path = os.path.join(ROOT, "profiles", f"tree_attention_verify_config{config}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path, encoding="utf-8") as fh:
+        for line in fh:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("attention_source_sha") != attn_source_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_worker(args):
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    w, req_ids, node_limit = args
+    from oracle import verify_step_ref
+    t0 = time.perf_counter()
+    nodes = 0
+    cu = np.asarray(w["cu_nodes"])
+    for b in req_ids:
+        n = int(cu[b + 1] - cu[b])
+        use = n if node_limit is None else min(n, node_limit)
+        sub = _sub_workload(w, b)
+        pairs = {0: [(i, h) for i in range(use) for h in range(w["num_q_heads"])]}
+        verify_step_ref(sub, sample=pairs)
+        nodes += use
+    return nodes, time.perf_counter() - t0
+
+
+def _sub_workload(w, b):
+    cu = np.asarray(w["cu_nodes"])
+    t0, t1 = int(cu[b]), int(cu[b + 1])
+    sub = dict(w)
+    sub.update(batch=1, cu_nodes=np.array([0, t1 - t0], np.int32),
+               parents=w["parents"][t0:t1], prompt_len=w["prompt_len"][b:b + 1],
+               draft_tokens=w["draft_tokens"][t0:t1], target_ids=w["target_ids"][t0:t1],
+               q=w["q"][t0:t1], k_new=w["k_new"][t0:t1], v_new=w["v_new"][t0:t1],
+               block_table=w["block_table"][b:b + 1], n_blocks=w["n_blocks"][b:b + 1])
+    return sub
+
+
+def cpu_baseline(w, seconds):
+    """Time the oracle (as it stands) on the host cores: one spawn worker per
+    core, single-threaded BLAS, each worker verifying whole requests."""
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    batch = w["batch"]
+    # calibrate on one request
+    n0, t_one = _oracle_worker((w, [0], None))
+    per_req = max(t_one, 1e-3)
+    reqs_total = max(1, int(seconds * cores / per_req))
+    order = [i % batch for i in range(reqs_total)]
+    chunks = [order[i::cores] for i in range(cores)]
+    chunks = [c for c in chunks if c]
+    t0 = time.perf_counter()
+    with ctx.Pool(len(chunks)) as pool:
+        res = pool.map(_oracle_worker, [(w, c, None) for c in chunks])
+    wall = time.perf_counter() - t0
+    nodes = sum(r[0] for r in res)
+    return {"value": nodes / wall, "unit": UNIT, "cores": len(chunks), "kind": "oracle",
+            "sample": f"{reqs_total} requests of the workload ({nodes} tree nodes, all query "
+                      f"heads, full step per request) over {len(chunks)} spawn workers, "
+                      f"{wall:.1f} s wall"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from speculative_decoding_tree_build_gb300 import workloads as wl
+    w = wl.make_config(args.config)
+    cores = os.cpu_count() or 1
+    # each step: one request's verification on the oracle; size so the run ends in minutes
+    n_first, t_first = _oracle_worker((w, [0], None))
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    node_limit = max(1, int(n_first * min(1.0, per_step / max(t_first, 1e-6))))
+    times, nodes = [], 0
+    for s in range(args.warmup + args.steps):
+        b = s % w["batch"]
+        n, dt = _oracle_worker((w, [b], node_limit))
+        if s >= args.warmup:
+            times.append(dt)
+            nodes += n
+    total = sum(times)
+    value = nodes / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step verifies {node_limit} node(s) (all query heads) "
+                                   f"of one request on the CPU oracle, single process"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "host_cores_available": cores,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from __graft_entry__ import build
+    build()
+    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from speculative_decoding_tree_build_gb300.step import DeviceBatch
+
+    w = wl.make_config(args.config, seed=1000 + args.config + 7919 * rank)
+    db = DeviceBatch(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    table0 = db.block_table.clone()
+    nblk0 = db.n_blocks.clone()
+    tokens_per_step = int(w["cu_nodes"][-1])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step(ev_attn=None):
+        db.block_table.copy_(table0, non_blocking=True)   # allocator refill
+        db.n_blocks.copy_(nblk0, non_blocking=True)
+        db.tree_build()
+        if ev_attn is not None:
+            ev_attn[0].record(stream)
+        db.attention()
+        if ev_attn is not None:
+            ev_attn[1].record(stream)
+        db.accept()
+        db.commit()
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    depth = db.depth.cpu().numpy()
+    st = db.status.cpu().numpy()
+    if np.any(st != 0):
+        raise RuntimeError(f"bench workload produced status flags {st}")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(ev_a[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    step_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_a]))
+
+    # end to end through the public API: host inputs in, results out
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {k: pin(getattr(db, k)) for k in ("parents", "cu_nodes", "prompt_len", "draft_tokens",
+                                                "target_ids", "q", "k_new", "v_new")}
+    h_out = {k: torch.empty_like(getattr(db, k), device="cpu").pin_memory()
+             for k in ("status", "accept_path", "accept_len", "bonus", "new_len", "released",
+                       "released_count")}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_steps = max(3, args.e2e_steps)
+    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        ev_e[i][0].record(stream)
+        for k, t in h_in.items():
+            getattr(db, k).copy_(t, non_blocking=True)
+        step()
+        for k, t in h_out.items():
+            t.copy_(getattr(db, k), non_blocking=True)
+        ev_e[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_e]))
+
+    vals = torch.tensor([step_ms, attn_ms, e2e_ms, float(tokens_per_step)], dtype=torch.float64,
+                        device=dev)
+    if world > 1:
+        mx = vals.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = vals.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        step_ms, attn_ms, e2e_ms = float(mx[0]), float(mx[1]), float(mx[2])
+        tokens_all = float(sm[3])
+    else:
+        tokens_all = float(tokens_per_step)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    nbytes, flops = attention_algorithmic(w, depth)
+    hbm_peak, tf_peak, src = measured_peaks()
+    attn_gbs = nbytes / (attn_ms * 1e-3) / 1e9
+    attn_tfs = flops / (attn_ms * 1e-3) / 1e12
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
+    bound = "hbm" if flops / nbytes < ridge else "tensor"
+    roof_s = max(nbytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": attn_gbs / hbm_peak}
+    else:
+        roof = {"bound": "tensor", "achieved": attn_tfs, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": attn_tfs / tf_peak}
+    roof.update(traffic=recorded_traffic(args.config), peak_source=src,
+                algorithmic_bytes=nbytes, algorithmic_flops=flops,
+                attention_us=attn_ms * 1e3, roofline_us=roof_s * 1e6,
+                frac_of_roofline_time=roof_s / (attn_ms * 1e-3),
+                frac_of_nominal_8tbs=attn_gbs / 8000.0)
+    line = {
+        "metric": METRIC, "value": tokens_all / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w), "roofline": roof,
+        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "attention_tokens_per_s": tokens_all / (attn_ms * 1e-3),
+        "clocks": clocks,
+    }
+    if world > 1:
+        dist.destroy_process_group()
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

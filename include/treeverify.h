@@ -1,0 +1,222 @@
+/*
+ * treeverify.h - C interface of the GB300 (sm_103a) token-tree verification
+ * library, libtreeverify.so.
+ *
+ * One verification step of tree speculative decoding runs four calls on the
+ * caller's CUDA stream:
+ *
+ *   tv_tree_build             parent list -> bit-packed ancestor mask, depth
+ *                             positions, retrieve_index / next_token /
+ *                             next_sibling
+ *   tv_tree_attention_verify  depth-RoPE of the tree's fresh Q/K, tentative KV
+ *                             write, GQA attention over the paged prompt cache
+ *                             plus each node's ancestors
+ *   tv_greedy_accept          longest accepted path + bonus token
+ *   tv_kv_commit              move the accepted K/V rows to the committed
+ *                             slots and release the blocks past the new end
+ *
+ * Sources of the definitions (web pages, cited by title and section):
+ *   [GLOSSARY] "Beam Search、约束解码与 Tree/Self Speculation"
+ *   [ATLAS]    "02 · Token Tree 与 Tree Attention"
+ *   [WIBLOG]   "投机解码的树状注意力验证：一次前向如何并行校验多条候选路径"
+ *   [DDTREE]   "Accelerating Speculative Decoding with Block Diffusion Draft Trees"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All array arguments are DEVICE pointers owned by the caller. The library
+ *    allocates no device memory, keeps no state between calls and never
+ *    synchronises the stream. Scratch space comes from the caller's workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - A batch holds `batch` requests whose nodes are concatenated:
+ *    request b owns flattened nodes [cu_nodes[b], cu_nodes[b+1]) (cu_nodes is
+ *    int32 [batch+1], cu_nodes[0] = 0, non-decreasing). Within a request node
+ *    0 is the root - the bonus token confirmed by the previous step, depth 0 -
+ *    and parent indices are local: parent[0] = -1, 0 <= parent[i] < i.
+ *    This topological packing is the packed layout of [GLOSSARY] section
+ *    "Packed tree attention" with the root of [ATLAS] §2 added as node 0.
+ *  - Paged KV pools k_cache / v_cache are bf16 [num_blocks][Hkv][16][D]
+ *    (block size 16). block_table is int32 [batch][max_blocks_per_req]:
+ *    slot s of request b lives in block block_table[b][s / 16], row s % 16.
+ *    n_blocks[b] is how many leading table entries request b holds.
+ *  - Return value: TV_OK or a negative TV_ERR_* code from host-side argument
+ *    checks (nothing is launched then). Errors in the DATA are reported per
+ *    request in `status` (int32 [batch], TV_ST_* flags); a request with a
+ *    non-zero status keeps its outputs untouched. No call traps or aborts.
+ *  - batch == 0 is a valid no-op.
+ */
+#ifndef TREEVERIFY_H_
+#define TREEVERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-side return codes */
+#define TV_OK 0
+#define TV_ERR_NULL_POINTER (-1)   /* a required pointer is NULL */
+#define TV_ERR_BAD_GEOMETRY (-2)   /* head_dim not 64/128, Hq % Hkv != 0, block_size != 16, bad rope */
+#define TV_ERR_BAD_SIZE (-3)       /* batch < 0, max_nodes outside [1, 1024], max_depth < 0, ... */
+#define TV_ERR_WORKSPACE (-4)      /* workspace smaller than tv_workspace_bytes() */
+#define TV_ERR_MISALIGNED (-5)     /* a bf16 array is not 16-byte aligned (workspace: 256) */
+#define TV_ERR_CUDA (-6)           /* a CUDA runtime/driver call failed */
+#define TV_ERR_DEVICE (-7)         /* the current device is not sm_103 */
+
+/* per-request status flags (OR-ed; 0 = fine) */
+#define TV_ST_BAD_SIZE 1           /* node count outside [1, max_nodes], prompt_len < 0, bad path */
+#define TV_ST_BAD_ROOT 2           /* parent[0] != -1 */
+#define TV_ST_BAD_PARENT 4         /* parent[i] outside [0, i-1] for some i >= 1 */
+#define TV_ST_BAD_BLOCK 8          /* a needed block-table entry is missing or out of range */
+#define TV_ST_PATH_OVERFLOW 16     /* accepted path longer than max_depth */
+#define TV_ST_TIMEOUT 32           /* a bounded device wait gave up (workspace must be re-zeroed) */
+
+#define TV_MAX_NODES 1024          /* largest tree (root included) per request */
+#define TV_BLOCK_SIZE 16
+
+typedef struct tv_geom {
+  int32_t num_q_heads;     /* Hq */
+  int32_t num_kv_heads;    /* Hkv; query head h reads KV head h / (Hq / Hkv) */
+  int32_t head_dim;        /* D: 64 or 128 */
+  int32_t block_size;      /* must be 16 */
+  float rope_base;         /* RoPE base (10000 in [GLOSSARY]'s experiment); > 0 */
+  float softmax_scale;     /* <= 0 means 1 / sqrt(D) ([GLOSSARY] packed_attention) */
+  int32_t rope_style;      /* 0: pairs (2i, 2i+1) as in [GLOSSARY]; 1: pairs (i, i + D/2) */
+} tv_geom;
+
+/*
+ * Workspace size for tv_tree_attention_verify on the CURRENT device.
+ * The workspace holds split-KV partial results and per-unit arrival
+ * counters. It must be zero-filled once before its first use; every call
+ * that finishes without TV_ST_TIMEOUT leaves it zero-filled again, so it can
+ * be reused by later calls on the same stream without clearing.
+ * Returns TV_OK and writes *bytes, or a TV_ERR_* code.
+ */
+int tv_workspace_bytes(const tv_geom* geom, int32_t batch, int32_t max_nodes, size_t* bytes);
+
+/*
+ * Tree metadata ([ATLAS] §3 "Tree attention 的 mask 规则": the builder turns
+ * the parent list into a tree mask, RoPE positions and retrieve_* arrays;
+ * positions = prompt length + depth, e.g. depths [0,1,1,2] with prompt 7 give
+ * [7,8,8,9]; [GLOSSARY] "Packed tree attention": each node sees its ancestor
+ * chain, never siblings or cousins).
+ *
+ *  parents        int32 [T]            local parent index per node (see above)
+ *  cu_nodes       int32 [batch+1]
+ *  prompt_len     int32 [batch]        committed tokens P_b already in the cache
+ *  max_nodes      largest node count allowed per request (1..1024); W = ceil(max_nodes/32)
+ *  mask_bits      uint32 [T][W] out    bit (j%32) of word j/32 of row t set iff
+ *                                      local node j is an ancestor of t or t itself
+ *  depth          int32 [T] out        root depth 0
+ *  positions      int32 [T] out        P_b + depth
+ *  retrieve_index int32 [T] out        flattened index of the node (cu_nodes[b] + i)
+ *  next_token     int32 [T] out        smallest-index child, -1 if none
+ *  next_sibling   int32 [T] out        next larger-index node with the same parent, -1 if none
+ *  status         int32 [batch] out    OVERWRITTEN: TV_ST_BAD_SIZE / _BAD_ROOT / _BAD_PARENT
+ *                                      or 0. Starts the step's per-request status.
+ */
+int tv_tree_build(const int32_t* parents, const int32_t* cu_nodes, const int32_t* prompt_len,
+                  int32_t batch, int32_t max_nodes, uint32_t* mask_bits, int32_t* depth,
+                  int32_t* positions, int32_t* retrieve_index, int32_t* next_token,
+                  int32_t* next_sibling, int32_t* status, void* stream);
+
+/*
+ * Packed tree attention with depth RoPE and the tentative KV write
+ * ([GLOSSARY] "Packed tree attention" and its packed-vs-branch experiment:
+ * softmax(q k^T * scale) v over the committed prefix plus the node's ancestor
+ * chain, RoPE at the node's depth position; [ATLAS] §3; [WIBLOG]
+ * "实现中的 KV Cache 与批处理约束": the tree's tentative KV occupies a contiguous
+ * region in node order).
+ *
+ *  q              bf16 [T][Hq][D]      raw (un-rotated) queries of the tree nodes
+ *  k_new, v_new   bf16 [T][Hkv][D]     raw keys / values of the tree nodes
+ *  cu_nodes       int32 [batch+1]
+ *  positions      int32 [T]            from tv_tree_build
+ *  mask_bits      uint32 [T][W]        from tv_tree_build (W = ceil(max_nodes/32))
+ *  prompt_len     int32 [batch]
+ *  block_table    int32 [batch][max_blocks_per_req], n_blocks int32 [batch]
+ *  k_cache,v_cache bf16 pools (see conventions). Slots [0, P_b) are read
+ *                 (already rotated); slots [P_b, P_b + N_b) receive the
+ *                 rotated k_new and the raw v_new of node i at slot P_b + i.
+ *                 Every block covering slots [0, P_b + N_b) must be held.
+ *  out            bf16 [T][Hq][D] out  attention output per node and query head
+ *  workspace      device scratch of tv_workspace_bytes() bytes (zeroed once)
+ *  status         int32 [batch] in/out requests whose status carries a tree
+ *                 flag are skipped; TV_ST_BAD_BLOCK / TV_ST_TIMEOUT are OR-ed in.
+ * Rotated K is rounded to bf16 (round-to-nearest-even) after an fp32
+ * rotation; scores and the softmax run in fp32 with bf16 tensor-core operands.
+ */
+int tv_tree_attention_verify(const tv_geom* geom, int32_t batch, int32_t max_nodes,
+                             const void* q, const void* k_new, const void* v_new,
+                             const int32_t* cu_nodes, const int32_t* positions,
+                             const uint32_t* mask_bits, const int32_t* prompt_len,
+                             const int32_t* block_table, const int32_t* n_blocks,
+                             int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                             int32_t num_blocks, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Greedy acceptance walk ([ATLAS] §4: from the root, move to the child whose
+ * token equals the target's choice, stop at the first miss, the target's
+ * token there is the correction / bonus; [GLOSSARY] three-part experiment
+ * verify_tree; [DDTREE] §6-§7.2). Among several matching children the
+ * smallest index wins.
+ *
+ *  target_ids     int32 [T]   target's greedy token after each node's prefix
+ *  draft_tokens   int32 [T]   token of each node (root: the previous bonus)
+ *  cu_nodes, next_token, next_sibling   as produced by tv_tree_build
+ *  max_nodes      as for tv_tree_build
+ *  max_depth      capacity of a path: accept_path rows hold max_depth + 1 entries
+ *  accept_path    int32 [batch][max_depth+1] out  local node indices from the root
+ *                 (entry 0 = 0), -1 after the last accepted node
+ *  accept_len     int32 [batch] out  accepted draft nodes a (path length a + 1)
+ *  bonus          int32 [batch] out  next step's root token
+ *  status         in/out: requests with non-zero status are skipped;
+ *                 TV_ST_PATH_OVERFLOW when a > max_depth (outputs untouched)
+ */
+int tv_greedy_accept(const int32_t* target_ids, const int32_t* draft_tokens,
+                     const int32_t* cu_nodes, const int32_t* next_token,
+                     const int32_t* next_sibling, int32_t batch, int32_t max_nodes,
+                     int32_t max_depth, int32_t* accept_path, int32_t* accept_len,
+                     int32_t* bonus, int32_t* status, void* stream);
+
+/*
+ * Commit / rollback of the tentative KV ([GLOSSARY] "Tree/Self Speculation":
+ * [10,11] becomes [10,11,4,7] and the other tentative nodes are released;
+ * [ATLAS] §4: the chosen path's KV is committed, the rest is discarded and
+ * pages are reclaimed; [WIBLOG]: with a paged cache reclaiming frees pages).
+ *
+ * For k = 1..a the K and V rows (all KV heads) of slot P+accept_path[k] move
+ * to slot P+k; every source row is read before any destination row of the
+ * same request is written. The bytes move unchanged: the row already carries
+ * RoPE at position P + k. new_len = P + 1 + a (the root is always kept).
+ * Held blocks with logical index >= ceil(new_len / 16) are released in
+ * ascending logical order: block_table entries become -1, n_blocks shrinks.
+ *
+ *  accept_path, accept_len    from tv_greedy_accept
+ *  block_table, n_blocks      in/out
+ *  new_len        int32 [batch] out
+ *  released       int32 [batch][max_blocks_per_req] out  released block ids,
+ *                 -1 after the last
+ *  released_count int32 [batch] out
+ *  status         in/out: requests with non-zero status are skipped;
+ *                 TV_ST_BAD_BLOCK / TV_ST_BAD_SIZE (invalid path) are OR-ed in.
+ */
+int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* accept_path,
+                 const int32_t* accept_len, int32_t max_depth, const int32_t* prompt_len,
+                 int32_t* block_table, int32_t* n_blocks, int32_t max_blocks_per_req,
+                 void* k_cache, void* v_cache, int32_t num_blocks, int32_t* new_len,
+                 int32_t* released, int32_t* released_count, int32_t* status, void* stream);
+
+/* Name of a TV_ERR_* code or of a single TV_ST_* flag. */
+const char* tv_status_string(int code);
+
+/* Library interface version (increments when a signature changes). */
+int tv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H_ */

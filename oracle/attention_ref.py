@@ -96,25 +96,21 @@ def gather_prompt_kv_ref(cache_bits, block_table_row, prompt_len, block_size=16)
     lives in block block_table_row[s // block_size] at row s % block_size.
     Returns float64 [P, Hkv, D].
     """
-    rows = []
-    for s in range(prompt_len):
-        blk = int(block_table_row[s // block_size])
-        rows.append(cache_bits[blk, :, s % block_size, :])
-    if not rows:
-        hkv, d = cache_bits.shape[1], cache_bits.shape[3]
-        return np.zeros((0, hkv, d), dtype=np.float64)
-    return bf16_bits_to_f64(np.stack(rows, axis=0))
+    slots = np.arange(prompt_len)
+    blocks = np.asarray(block_table_row)[slots // block_size].astype(np.int64)
+    rows = cache_bits[blocks, :, slots % block_size, :]          # [P, Hkv, D]
+    return bf16_bits_to_f64(rows)
 
 
 def tree_attention_verify_ref(q_rot, k_tree_rot, v_tree, parents, k_cache_bits,
                               v_cache_bits, block_table_row, prompt_len,
-                              block_size=16, scale=None, nodes=None, heads=None):
+                              block_size=16, scale=None, pairs=None):
     """Attention outputs of one request (float64, not rounded).
 
     q_rot [N, Hq, D], k_tree_rot/v_tree [N, Hkv, D] are float64 (the rotated,
     bf16-rounded values); the prompt K/V are read from the paged pools.
-    ``nodes``/``heads`` optionally restrict which (node, q-head) outputs are
-    computed (others are NaN), for sampled checks at large sizes.
+    ``pairs`` optionally restricts the computed (node, q_head) outputs (the
+    others are NaN), for sampled checks at large sizes.
     """
     kp = gather_prompt_kv_ref(k_cache_bits, block_table_row, prompt_len, block_size)
     vp = gather_prompt_kv_ref(v_cache_bits, block_table_row, prompt_len, block_size)
@@ -123,15 +119,14 @@ def tree_attention_verify_ref(q_rot, k_tree_rot, v_tree, parents, k_cache_bits,
     group = hq // hkv
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    node_list = range(n) if nodes is None else nodes
-    head_list = range(hq) if heads is None else heads
+    if pairs is None:
+        pairs = [(i, h) for i in range(n) for h in range(hq)]
     out = np.full((n, hq, d), np.nan, dtype=np.float64)
-    for i in node_list:
+    for i, h in pairs:
         chain = ancestor_path(parents, i)
-        for h in head_list:
-            g = h // group
-            keys = np.concatenate([kp[:, g, :], k_tree_rot[chain, g, :]], axis=0)
-            vals = np.concatenate([vp[:, g, :], v_tree[chain, g, :]], axis=0)
-            p = _softmax((keys @ q_rot[i, h]) * scale)
-            out[i, h] = p @ vals
+        g = h // group
+        keys = np.concatenate([kp[:, g, :], k_tree_rot[chain, g, :]], axis=0)
+        vals = np.concatenate([vp[:, g, :], v_tree[chain, g, :]], axis=0)
+        p = _softmax((keys @ q_rot[i, h]) * scale)
+        out[i, h] = p @ vals
     return out

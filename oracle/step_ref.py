@@ -108,19 +108,11 @@ def verify_step_ref(w, attention=True, sample=None, commit=True):
         v_new = bf16_bits_to_f64(w["v_new"][t0:t1])
         res["k_rot_bits"][t0:t1] = f64_to_bf16_bits(k_rot)
         if attention:
-            nodes = heads = None
-            if sample is not None:
-                pairs = sample.get(b, [])
-                if pairs:
-                    for (i, h) in pairs:
-                        o = tree_attention_verify_ref(
-                            q_rot, k_rot, v_new, parents, k_cache, v_cache, row, plen,
-                            bs, nodes=[i], heads=[h])
-                        res["out"][t0 + i, h] = o[i, h]
-            else:
+            pairs = None if sample is None else sample.get(b, [])
+            if pairs is None or pairs:
                 res["out"][t0:t1] = tree_attention_verify_ref(
                     q_rot, k_rot, v_new, parents, k_cache, v_cache, row, plen, bs,
-                    nodes=nodes, heads=heads)
+                    pairs=pairs)
         # Tentative write of the rotated K and raw V into slots P + i.
         for i in range(n):
             s = plen + i

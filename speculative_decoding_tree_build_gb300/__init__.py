@@ -1,0 +1,177 @@
+"""Python binding of libtreeverify (GB300 token-tree verification).
+
+The functions below carry the names of the C entry points declared in
+``include/treeverify.h`` and only marshal arguments: torch tensors are checked
+for device, dtype and contiguity and passed as raw device pointers together
+with the current CUDA stream. Every step of the verification runs in the
+library's CUDA kernels; there is no CPU fallback. If the shared library has
+not been built, ``load()`` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
+    "tree_build", "tree_attention_verify", "greedy_accept", "kv_commit", "status_string",
+    "version",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libtreeverify.so")
+
+TV_OK = 0
+TV_ST = {"BAD_SIZE": 1, "BAD_ROOT": 2, "BAD_PARENT": 4, "BAD_BLOCK": 8,
+         "PATH_OVERFLOW": 16, "TIMEOUT": 32}
+
+
+class TvGeom(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("rope_base", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+                ("rope_style", ctypes.c_int32)]
+
+
+class TvError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "tv_workspace_bytes": [ctypes.POINTER(TvGeom), _I, _I, ctypes.POINTER(_SZ)],
+    "tv_tree_build": [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P],
+    "tv_tree_attention_verify": [ctypes.POINTER(TvGeom), _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                 _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P, _P],
+    "tv_greedy_accept": [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P],
+    "tv_kv_commit": [ctypes.POINTER(TvGeom), _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
+                     _P, _P, _P, _P],
+    "tv_status_string": [ctypes.c_int],
+    "tv_version": [],
+}
+
+
+def load(path: str | None = None):
+    """Load libtreeverify.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or lib_path
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} is missing: build it with `python -m speculative_decoding_tree_build_gb300.build` "
+            "(or __graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(p)
+    for name, args in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "tv_status_string" else ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().tv_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return load().tv_version()
+
+
+def geom(num_q_heads, num_kv_heads, head_dim, block_size=16, rope_base=10000.0,
+         softmax_scale=0.0, rope_style=0) -> TvGeom:
+    return TvGeom(num_q_heads, num_kv_heads, head_dim, block_size, rope_base, softmax_scale,
+                  rope_style)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != TV_OK:
+        raise TvError(fn, rc)
+    return rc
+
+
+I32, U32, BF16 = torch.int32, torch.uint32 if hasattr(torch, "uint32") else torch.int32, torch.bfloat16
+
+
+def workspace_bytes(g: TvGeom, batch: int, max_nodes: int) -> int:
+    out = _SZ(0)
+    _check("tv_workspace_bytes", load().tv_workspace_bytes(ctypes.byref(g), batch, max_nodes,
+                                                           ctypes.byref(out)))
+    return out.value
+
+
+def tree_build(parents, cu_nodes, prompt_len, max_nodes, mask_bits, depth, positions,
+               retrieve_index, next_token, next_sibling, status, stream=None):
+    batch = cu_nodes.numel() - 1
+    return _check("tv_tree_build", load().tv_tree_build(
+        _ptr(parents, I32, "parents"), _ptr(cu_nodes, I32, "cu_nodes"),
+        _ptr(prompt_len, I32, "prompt_len"), batch, max_nodes, _ptr(mask_bits, None, "mask_bits"),
+        _ptr(depth, I32), _ptr(positions, I32), _ptr(retrieve_index, I32), _ptr(next_token, I32),
+        _ptr(next_sibling, I32), _ptr(status, I32, "status"), _stream(stream)))
+
+
+def tree_attention_verify(g: TvGeom, max_nodes, q, k_new, v_new, cu_nodes, positions, mask_bits,
+                          prompt_len, block_table, n_blocks, k_cache, v_cache, out, workspace,
+                          status, stream=None):
+    batch = cu_nodes.numel() - 1
+    return _check("tv_tree_attention_verify", load().tv_tree_attention_verify(
+        ctypes.byref(g), batch, max_nodes, _ptr(q, BF16, "q"), _ptr(k_new, BF16, "k_new"),
+        _ptr(v_new, BF16, "v_new"), _ptr(cu_nodes, I32), _ptr(positions, I32),
+        _ptr(mask_bits, None), _ptr(prompt_len, I32), _ptr(block_table, I32, "block_table"),
+        _ptr(n_blocks, I32), block_table.shape[1], _ptr(k_cache, BF16, "k_cache"),
+        _ptr(v_cache, BF16, "v_cache"), k_cache.shape[0], _ptr(out, BF16, "out"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(status, I32), _stream(stream)))
+
+
+def greedy_accept(target_ids, draft_tokens, cu_nodes, next_token, next_sibling, max_nodes,
+                  accept_path, accept_len, bonus, status, stream=None):
+    batch = cu_nodes.numel() - 1
+    max_depth = accept_path.shape[1] - 1
+    return _check("tv_greedy_accept", load().tv_greedy_accept(
+        _ptr(target_ids, I32, "target_ids"), _ptr(draft_tokens, I32, "draft_tokens"),
+        _ptr(cu_nodes, I32), _ptr(next_token, I32), _ptr(next_sibling, I32), batch, max_nodes,
+        max_depth, _ptr(accept_path, I32), _ptr(accept_len, I32), _ptr(bonus, I32),
+        _ptr(status, I32), _stream(stream)))
+
+
+def kv_commit(g: TvGeom, accept_path, accept_len, prompt_len, block_table, n_blocks, k_cache,
+              v_cache, new_len, released, released_count, status, stream=None):
+    batch = accept_len.numel()
+    return _check("tv_kv_commit", load().tv_kv_commit(
+        ctypes.byref(g), batch, _ptr(accept_path, I32), _ptr(accept_len, I32),
+        accept_path.shape[1] - 1, _ptr(prompt_len, I32), _ptr(block_table, I32),
+        _ptr(n_blocks, I32), block_table.shape[1], _ptr(k_cache, BF16), _ptr(v_cache, BF16),
+        k_cache.shape[0], _ptr(new_len, I32), _ptr(released, I32), _ptr(released_count, I32),
+        _ptr(status, I32), _stream(stream)))

@@ -1,0 +1,104 @@
+// tv_greedy_accept: greedy walk of the candidate tree against the target's
+// per-node greedy tokens.
+//
+// Definition: "02 · Token Tree 与 Tree Attention" §4 (from the root accept the
+// child whose token equals the target's choice and continue from it; when no
+// child matches the target's token is the correction), "Beam Search、约束解码与
+// Tree/Self Speculation" three-part experiment (verify_tree keeps the branches
+// matching the target at each depth and stops at the first miss) and
+// "Accelerating Speculative Decoding with Block Diffusion Draft Trees" §7.2
+// (the first mismatching target token becomes the next bonus token).
+//
+// One CTA per request: the request's arrays are staged into shared memory
+// with coalesced loads, then one thread walks first-child / next-sibling links
+// there (shared-memory latency instead of a chain of dependent global loads).
+#include "tv_common.cuh"
+
+namespace tv {
+
+constexpr int kAcceptThreads = 128;
+
+__global__ void __launch_bounds__(kAcceptThreads)
+greedy_accept_kernel(const int32_t* __restrict__ target_ids,
+                     const int32_t* __restrict__ draft_tokens,
+                     const int32_t* __restrict__ cu_nodes, const int32_t* __restrict__ next_token,
+                     const int32_t* __restrict__ next_sibling, int max_nodes, int max_depth,
+                     int32_t* __restrict__ accept_path, int32_t* __restrict__ accept_len,
+                     int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
+  __shared__ int s_tgt[TV_MAX_NODES];
+  __shared__ int s_tok[TV_MAX_NODES];
+  __shared__ int s_first[TV_MAX_NODES];
+  __shared__ int s_next[TV_MAX_NODES];
+  __shared__ int s_path[TV_MAX_NODES];
+  __shared__ int s_len, s_bonus, s_bad;
+  const int b = blockIdx.x;
+  if (status[b] != 0) return;
+  const int t0 = cu_nodes[b];
+  const int n = cu_nodes[b + 1] - t0;
+  if (n < 1 || n > max_nodes) {
+    if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
+    return;
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    s_tgt[i] = target_ids[t0 + i];
+    s_tok[i] = draft_tokens[t0 + i];
+    s_first[i] = next_token[t0 + i];
+    s_next[i] = next_sibling[t0 + i];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int len = 0, cur = 0, bad = 0;
+    s_path[0] = 0;
+    while (true) {
+      const int want = s_tgt[cur];
+      int c = s_first[cur];
+      int guard = 0;
+      while (c != -1 && s_tok[c] != want) {
+        c = s_next[c];
+        // links come from tv_tree_build; a corrupted list must not loop or
+        // index outside the request
+        if (c >= n || c < -1 || ++guard > n) { bad = 1; break; }
+      }
+      if (bad || c == -1) {
+        s_bonus = want;
+        break;
+      }
+      if (c <= cur || c >= n || len + 1 >= n) { bad = 1; break; }
+      s_path[++len] = c;
+      cur = c;
+    }
+    s_len = len;
+    s_bad = bad ? TV_ST_BAD_SIZE : (len > max_depth ? TV_ST_PATH_OVERFLOW : 0);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) atomicOr(&status[b], s_bad);
+    return;
+  }
+  const int len = s_len;
+  int32_t* row = accept_path + static_cast<size_t>(b) * (max_depth + 1);
+  for (int k = threadIdx.x; k <= max_depth; k += blockDim.x) row[k] = k <= len ? s_path[k] : -1;
+  if (threadIdx.x == 0) {
+    accept_len[b] = len;
+    bonus[b] = s_bonus;
+  }
+}
+
+}  // namespace tv
+
+extern "C" int tv_greedy_accept(const int32_t* target_ids, const int32_t* draft_tokens,
+                                const int32_t* cu_nodes, const int32_t* next_token,
+                                const int32_t* next_sibling, int32_t batch, int32_t max_nodes,
+                                int32_t max_depth, int32_t* accept_path, int32_t* accept_len,
+                                int32_t* bonus, int32_t* status, void* stream) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > TV_MAX_NODES || max_depth < 0)
+    return TV_ERR_BAD_SIZE;
+  if (batch == 0) return TV_OK;
+  if (!target_ids || !draft_tokens || !cu_nodes || !next_token || !next_sibling ||
+      !accept_path || !accept_len || !bonus || !status)
+    return TV_ERR_NULL_POINTER;
+  tv::greedy_accept_kernel<<<batch, tv::kAcceptThreads, 0, tv::as_stream(stream)>>>(
+      target_ids, draft_tokens, cu_nodes, next_token, next_sibling, max_nodes, max_depth,
+      accept_path, accept_len, bonus, status);
+  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}

@@ -1,0 +1,157 @@
+// tv_kv_commit: move the accepted path's tentative K/V rows to the committed
+// slots and release the blocks past the new end.
+//
+// Definition: "Beam Search、约束解码与 Tree/Self Speculation" section
+// "Tree/Self Speculation" ([10,11] -> [10,11,4,7]; every other tentative node
+// is rolled back), "02 · Token Tree 与 Tree Attention" §4 (the chosen path's KV
+// becomes the next round's prompt, the rest is discarded, pages are
+// reclaimed) and "投机解码的树状注意力验证…" section "实现中的 KV Cache 与批处理约束"
+// (a contiguous tree region in node order; a paged cache frees or reuses
+// pages).
+//
+// Slot P+path[k] moves to slot P+k for k = 1..a. path[k] >= k, so a
+// destination slot can be the source of an EARLIER k only. The rows are
+// therefore moved in ascending chunks, each chunk staged in shared memory
+// (all of its reads before any of its writes); later chunks only read slots
+// that no earlier chunk wrote. One CTA per request; byte moves are exact.
+#include "tv_common.cuh"
+
+namespace tv {
+
+constexpr int kCommitThreads = 256;
+constexpr int kCommitSmem = 64 * 1024;
+
+__global__ void __launch_bounds__(kCommitThreads)
+kv_commit_kernel(const int32_t* __restrict__ accept_path, const int32_t* __restrict__ accept_len,
+                 int max_depth, const int32_t* __restrict__ prompt_len,
+                 int32_t* __restrict__ block_table, int32_t* __restrict__ n_blocks,
+                 int max_blocks, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                 int num_blocks, int hkv, int head_vecs, int32_t* __restrict__ new_len,
+                 int32_t* __restrict__ released, int32_t* __restrict__ released_count,
+                 int32_t* __restrict__ status) {
+  extern __shared__ uint4 stage[];
+  __shared__ int s_path[TV_MAX_NODES];
+  __shared__ int s_blk[2 * TV_MAX_NODES];
+  __shared__ int s_bad;
+  const int b = blockIdx.x;
+  if (status[b] != 0) return;
+  const int a = accept_len[b];
+  const int plen = prompt_len[b];
+  if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0) {
+    if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
+    return;
+  }
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const int32_t* path = accept_path + static_cast<size_t>(b) * (max_depth + 1);
+  const int32_t* table = block_table + static_cast<size_t>(b) * max_blocks;
+  const int held = n_blocks[b];
+  for (int k = threadIdx.x; k <= a; k += blockDim.x) s_path[k] = path[k];
+  __syncthreads();
+  int bad = 0;
+  for (int k = threadIdx.x; k <= a; k += blockDim.x) {
+    const int pk = s_path[k];
+    if (k == 0) {
+      if (pk != 0) bad |= TV_ST_BAD_SIZE;
+      continue;
+    }
+    if (pk <= s_path[k - 1]) { bad |= TV_ST_BAD_SIZE; continue; }
+    // source and destination blocks of row k
+    const long long src = static_cast<long long>(plen) + pk, dst = plen + k;
+    const long long lbs = src / TV_BLOCK_SIZE, lbd = dst / TV_BLOCK_SIZE;
+    int bs = -1, bd = -1;
+    if (lbs < held && lbs < max_blocks) bs = table[lbs];
+    if (lbd < held && lbd < max_blocks) bd = table[lbd];
+    if (bs < 0 || bs >= num_blocks || bd < 0 || bd >= num_blocks) bad |= TV_ST_BAD_BLOCK;
+    s_blk[2 * k] = bs;
+    s_blk[2 * k + 1] = bd;
+  }
+  if (bad) atomicOr(&s_bad, bad);
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) atomicOr(&status[b], s_bad);
+    return;
+  }
+
+  // rows to move (skip k with path[k] == k: already in place)
+  const int row_vecs = 2 * hkv * head_vecs;   // K and V, all heads
+  const int chunk_rows = kCommitSmem / (row_vecs * 16);
+  for (int k0 = 1; k0 <= a; k0 += chunk_rows) {
+    const int k1 = min(a + 1, k0 + chunk_rows);
+    const int total = (k1 - k0) * row_vecs;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+      const int r = e / row_vecs, rem = e % row_vecs;
+      const int k = k0 + r;
+      if (s_path[k] == k) continue;
+      const int kv = rem / (hkv * head_vecs), h = (rem / head_vecs) % hkv, v = rem % head_vecs;
+      const int slot = (plen + s_path[k]) % TV_BLOCK_SIZE;
+      const size_t idx = ((static_cast<size_t>(s_blk[2 * k]) * hkv + h) * TV_BLOCK_SIZE + slot) *
+                             head_vecs + v;
+      stage[e] = kv ? v_cache[idx] : k_cache[idx];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+      const int r = e / row_vecs, rem = e % row_vecs;
+      const int k = k0 + r;
+      if (s_path[k] == k) continue;
+      const int kv = rem / (hkv * head_vecs), h = (rem / head_vecs) % hkv, v = rem % head_vecs;
+      const int slot = (plen + k) % TV_BLOCK_SIZE;
+      const size_t idx = ((static_cast<size_t>(s_blk[2 * k + 1]) * hkv + h) * TV_BLOCK_SIZE + slot) *
+                             head_vecs + v;
+      if (kv) v_cache[idx] = stage[e]; else k_cache[idx] = stage[e];
+    }
+    __syncthreads();
+  }
+
+  // release the blocks past the new end
+  const long long nl = static_cast<long long>(plen) + 1 + a;
+  const int keep = static_cast<int>((nl + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
+  const int count = held > keep ? held - keep : 0;
+  int32_t* trow = block_table + static_cast<size_t>(b) * max_blocks;
+  int32_t* rrow = released + static_cast<size_t>(b) * max_blocks;
+  for (int j = threadIdx.x; j < max_blocks; j += blockDim.x) {
+    if (j < count && keep + j < max_blocks) {
+      rrow[j] = trow[keep + j];
+      trow[keep + j] = -1;
+    } else {
+      rrow[j] = -1;
+    }
+  }
+  if (threadIdx.x == 0) {
+    new_len[b] = static_cast<int>(nl);
+    released_count[b] = count;
+    n_blocks[b] = held < keep ? held : keep;
+  }
+}
+
+}  // namespace tv
+
+extern "C" int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* accept_path,
+                            const int32_t* accept_len, int32_t max_depth,
+                            const int32_t* prompt_len, int32_t* block_table, int32_t* n_blocks,
+                            int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                            int32_t num_blocks, int32_t* new_len, int32_t* released,
+                            int32_t* released_count, int32_t* status, void* stream) {
+  int rc = tv::check_geom(geom);
+  if (rc != TV_OK) return rc;
+  if (batch < 0 || max_depth < 0 || max_blocks_per_req < 1 || num_blocks < 1)
+    return TV_ERR_BAD_SIZE;
+  if (batch == 0) return TV_OK;
+  if (!accept_path || !accept_len || !prompt_len || !block_table || !n_blocks || !k_cache ||
+      !v_cache || !new_len || !released || !released_count || !status)
+    return TV_ERR_NULL_POINTER;
+  if (!tv::aligned(k_cache, 16) || !tv::aligned(v_cache, 16)) return TV_ERR_MISALIGNED;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(tv::kv_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tv::kCommitSmem) != cudaSuccess)
+      return TV_ERR_CUDA;
+    configured = true;
+  }
+  const int head_vecs = geom->head_dim / 8;
+  tv::kv_commit_kernel<<<batch, tv::kCommitThreads, tv::kCommitSmem, tv::as_stream(stream)>>>(
+      accept_path, accept_len, max_depth, prompt_len, block_table, n_blocks, max_blocks_per_req,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks,
+      geom->num_kv_heads, head_vecs, new_len, released, released_count, status);
+  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}

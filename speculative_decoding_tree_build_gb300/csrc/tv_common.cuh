@@ -1,0 +1,57 @@
+// Shared device/host helpers of libtreeverify (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/treeverify.h"
+
+#define TV_TREE_FLAGS (TV_ST_BAD_SIZE | TV_ST_BAD_ROOT | TV_ST_BAD_PARENT)
+
+namespace tv {
+
+// ---------------------------------------------------------------- host side
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline int check_geom(const tv_geom* g) {
+  if (g == nullptr) return TV_ERR_NULL_POINTER;
+  if (g->head_dim != 64 && g->head_dim != 128) return TV_ERR_BAD_GEOMETRY;
+  if (g->num_kv_heads < 1 || g->num_q_heads < 1) return TV_ERR_BAD_GEOMETRY;
+  if (g->num_q_heads % g->num_kv_heads != 0) return TV_ERR_BAD_GEOMETRY;
+  if (g->num_q_heads / g->num_kv_heads > 16) return TV_ERR_BAD_GEOMETRY;
+  if (g->block_size != TV_BLOCK_SIZE) return TV_ERR_BAD_GEOMETRY;
+  if (!(g->rope_base > 0.0f)) return TV_ERR_BAD_GEOMETRY;
+  if (g->rope_style != 0 && g->rope_style != 1) return TV_ERR_BAD_GEOMETRY;
+  return TV_OK;
+}
+
+// --------------------------------------------------------------- device side
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Pack two floats into a bf16x2 word (lo in bits 0..15), round-to-nearest-even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace tv

@@ -1,0 +1,113 @@
+"""Device buffers for one batch and the four library calls of a verification
+step, in order (tree_build -> tree_attention_verify -> greedy_accept ->
+kv_commit). torch only provides device memory and the stream."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (geom as make_geom, greedy_accept, kv_commit, tree_attention_verify, tree_build,
+               workspace_bytes)
+
+_STEP_INPUTS = ("parents", "cu_nodes", "prompt_len", "draft_tokens", "target_ids")
+
+
+def _i32(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+
+def _bf16(bits, dev):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(dev).view(torch.bfloat16)
+
+
+class DeviceBatch:
+    """A workload dict (see workloads.py) resident on a CUDA device, plus the
+    output buffers and the attention workspace."""
+
+    def __init__(self, w, device="cuda", workspace=None):
+        dev = torch.device(device)
+        self.w = w
+        self.device = dev
+        self.g = make_geom(w["num_q_heads"], w["num_kv_heads"], w["head_dim"], w["block_size"],
+                           w["rope_base"], 0.0, w["rope_style"])
+        self.max_nodes = int(w["max_nodes"])
+        self.max_depth = int(w["max_depth"])
+        self.batch = int(w["batch"])
+        self.k_cache = _bf16(w["k_cache"], dev)
+        self.v_cache = _bf16(w["v_cache"], dev)
+        self.block_table = _i32(w["block_table"], dev)
+        self.n_blocks = _i32(w["n_blocks"], dev)
+        self.load_step_inputs(w)
+        ws = workspace_bytes(self.g, self.batch, self.max_nodes)
+        if workspace is None:
+            workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        self.status = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.accept_path = torch.zeros(self.batch, self.max_depth + 1, dtype=torch.int32, device=dev)
+        self.accept_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.bonus = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.new_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.released = torch.zeros(self.batch, self.block_table.shape[1], dtype=torch.int32, device=dev)
+        self.released_count = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+
+    def load_step_inputs(self, w):
+        """(Re)load the per-step inputs (tree, tokens, fresh Q/K/V) and size
+        the per-node outputs."""
+        dev = self.device
+        self.parents = _i32(w["parents"], dev)
+        self.cu_nodes = _i32(w["cu_nodes"], dev)
+        self.prompt_len = _i32(w["prompt_len"], dev)
+        self.draft_tokens = _i32(w["draft_tokens"], dev)
+        self.target_ids = _i32(w["target_ids"], dev)
+        self.q = _bf16(w["q"], dev)
+        self.k_new = _bf16(w["k_new"], dev)
+        self.v_new = _bf16(w["v_new"], dev)
+        total = int(w["cu_nodes"][-1])
+        words = (self.max_nodes + 31) // 32
+        self.mask = torch.zeros(total, words, dtype=torch.int32, device=dev)
+        self.depth = torch.zeros(total, dtype=torch.int32, device=dev)
+        self.positions = torch.zeros(total, dtype=torch.int32, device=dev)
+        self.retrieve_index = torch.zeros(total, dtype=torch.int32, device=dev)
+        self.next_token = torch.zeros(total, dtype=torch.int32, device=dev)
+        self.next_sibling = torch.zeros(total, dtype=torch.int32, device=dev)
+        self.out = torch.zeros(total, w["num_q_heads"], w["head_dim"], dtype=torch.bfloat16,
+                               device=dev)
+
+    # the four calls -----------------------------------------------------
+    def tree_build(self, stream=None):
+        tree_build(self.parents, self.cu_nodes, self.prompt_len, self.max_nodes, self.mask,
+                   self.depth, self.positions, self.retrieve_index, self.next_token,
+                   self.next_sibling, self.status, stream)
+
+    def attention(self, stream=None):
+        tree_attention_verify(self.g, self.max_nodes, self.q, self.k_new, self.v_new,
+                              self.cu_nodes, self.positions, self.mask, self.prompt_len,
+                              self.block_table, self.n_blocks, self.k_cache, self.v_cache,
+                              self.out, self.workspace, self.status, stream)
+
+    def accept(self, stream=None):
+        greedy_accept(self.target_ids, self.draft_tokens, self.cu_nodes, self.next_token,
+                      self.next_sibling, self.max_nodes, self.accept_path, self.accept_len,
+                      self.bonus, self.status, stream)
+
+    def commit(self, stream=None):
+        kv_commit(self.g, self.accept_path, self.accept_len, self.prompt_len, self.block_table,
+                  self.n_blocks, self.k_cache, self.v_cache, self.new_len, self.released,
+                  self.released_count, self.status, stream)
+
+    def step(self, stream=None):
+        self.tree_build(stream)
+        self.attention(stream)
+        self.accept(stream)
+        self.commit(stream)
+
+    # host views -----------------------------------------------------------
+    def cache_bits(self):
+        k = self.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+        v = self.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+        return k, v
+
+    def out_f32(self):
+        return self.out.float().cpu().numpy()

@@ -1,0 +1,150 @@
+"""Helpers for the GPU parity tests: run the library on a workload and compare
+with the oracle on the same seeded inputs."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import bf16_bits_to_f64, verify_step_ref
+from speculative_decoding_tree_build_gb300.step import DeviceBatch
+
+ATOL = 2e-2          # max-abs error bound for bf16-input, fp32-accumulate attention
+REL_FRO = 5e-3       # relative Frobenius error bound
+
+
+def sample_pairs(w, per_request, seed=0):
+    """(node, q_head) samples per request: the root, the deepest node, the
+    last node and random ones."""
+    rng = np.random.default_rng(seed)
+    cu = w["cu_nodes"]
+    hq = w["num_q_heads"]
+    out = {}
+    for b in range(w["batch"]):
+        n = int(cu[b + 1] - cu[b])
+        nodes = {0, n - 1} | set(rng.integers(0, n, size=per_request).tolist())
+        pairs = set()
+        for i in nodes:
+            pairs.add((int(i), int(rng.integers(0, hq))))
+            pairs.add((int(i), hq - 1))
+        out[b] = sorted(pairs)
+    return out
+
+
+def compare_out(gpu_out, ref_out, w, pairs=None):
+    """Element-wise attention comparison on all (or the sampled) outputs."""
+    cu = w["cu_nodes"]
+    g_list, r_list = [], []
+    for b in range(w["batch"]):
+        t0 = int(cu[b])
+        if pairs is None:
+            n = int(cu[b + 1] - cu[b])
+            g_list.append(gpu_out[t0:t0 + n].reshape(-1))
+            r_list.append(ref_out[t0:t0 + n].reshape(-1))
+        else:
+            for (i, h) in pairs.get(b, []):
+                g_list.append(gpu_out[t0 + i, h])
+                r_list.append(ref_out[t0 + i, h])
+    g = np.concatenate(g_list).astype(np.float64)
+    r = np.concatenate(r_list)
+    assert np.all(np.isfinite(r)) and np.all(np.isfinite(g))
+    max_abs = float(np.max(np.abs(g - r)))
+    rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
+    assert max_abs <= ATOL, f"max abs error {max_abs:.3e} > {ATOL}"
+    assert rel <= REL_FRO, f"relative Frobenius error {rel:.3e} > {REL_FRO}"
+    return max_abs, rel
+
+
+def bf16_ulp_diff(a_bits, b_bits):
+    """Distance in bf16 units in the last place between two bit arrays."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, 0x8000 - (x & 0x7FFF), x + 0x8000)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def rope_close(gpu_bits, x_raw, positions, w):
+    """Rotated keys from the GPU against the exact rotation of the same raw
+    keys. The GPU rotates in float32 then rounds to bf16, so each value may
+    differ from the exact one by one bf16 ulp plus the float32 rotation's
+    absolute error (a few 2**-24 * (|a| + |b|) for the pair (a, b); large
+    relative to the value when a*cos - b*sin nearly cancels)."""
+    from oracle import rope_ref
+    exact = rope_ref(x_raw, positions, w["rope_base"], w["rope_style"], round_bf16=False)
+    d = x_raw.shape[-1]
+    if w["rope_style"] == 0:
+        pair = np.abs(x_raw[..., 0::2]) + np.abs(x_raw[..., 1::2])
+        pair = np.repeat(pair, 2, axis=-1)
+    else:
+        half = np.abs(x_raw[..., : d // 2]) + np.abs(x_raw[..., d // 2:])
+        pair = np.concatenate([half, half], axis=-1)
+    got = bf16_bits_to_f64(gpu_bits)
+    _, e = np.frexp(exact)
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    err = np.abs(got - exact)
+    tol = ulp + 2.0 ** -20 * pair
+    bad = err > tol
+    if np.any(bad):
+        i = int(np.argmax(err - tol))
+        raise AssertionError(
+            f"rotated key off: got {got.ravel()[i]!r} exact {exact.ravel()[i]!r} "
+            f"pair |a|+|b| {pair.ravel()[i]!r} ({int(bad.sum())} of {bad.size})")
+    return float(np.max(err))
+
+
+def tentative_rows(pool_bits, w, b, n, block_table=None):
+    """Rows of slots [P_b, P_b + n) of request b: [n, Hkv, D]."""
+    bs = w["block_size"]
+    table = w["block_table"] if block_table is None else block_table
+    plen = int(w["prompt_len"][b])
+    slots = np.arange(plen, plen + n)
+    return pool_bits[table[b][slots // bs].astype(np.int64), :, slots % bs, :]
+
+
+def run_gpu(w, calls=("build", "attn", "accept", "commit"), db=None):
+    db = db or DeviceBatch(w)
+    for c in calls:
+        {"build": db.tree_build, "attn": db.attention, "accept": db.accept,
+         "commit": db.commit}[c]()
+    torch.cuda.synchronize()
+    return db
+
+
+def check_tree_outputs(db, ref, w):
+    cu = w["cu_nodes"]
+    st = db.status.cpu().numpy()
+    assert np.array_equal(st & 7, ref["status"] & 7)
+    for b in range(w["batch"]):
+        if ref["status"][b] & 7:
+            continue
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        for k in ("depth", "positions", "retrieve_index", "next_token", "next_sibling"):
+            got = getattr(db, k)[t0:t1].cpu().numpy()
+            assert np.array_equal(got, ref[k][t0:t1]), k
+        got = db.mask[t0:t1].cpu().numpy().view(np.uint32)
+        assert np.array_equal(got, ref["mask"][t0:t1])
+
+
+def check_accept_outputs(db, ref, w):
+    st = db.status.cpu().numpy()
+    paths = db.accept_path.cpu().numpy()
+    lens = db.accept_len.cpu().numpy()
+    bonus = db.bonus.cpu().numpy()
+    for b in range(w["batch"]):
+        if ref["paths"][b] is None:
+            continue
+        path = ref["paths"][b]
+        assert st[b] == 0
+        assert lens[b] == len(path) - 1 and bonus[b] == ref["bonus"][b]
+        want = np.full(paths.shape[1], -1)
+        want[:len(path)] = path
+        assert np.array_equal(paths[b], want)
+
+
+def oracle_step(w, sample=None, commit=True):
+    return verify_step_ref(w, sample=sample, commit=commit)
+
+
+__all__ = ["ATOL", "REL_FRO", "sample_pairs", "compare_out", "bf16_ulp_diff", "tentative_rows",
+           "run_gpu", "rope_close", "check_tree_outputs", "check_accept_outputs", "oracle_step",
+           "bf16_bits_to_f64"]

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/treeverify.h declares, and rejects bad arguments on the host before
+touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_tree_build_gb300 as tv
+from speculative_decoding_tree_build_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return tv.load()
+
+
+def header_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_step_calls():
+    names = header_functions()
+    for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
+                 "tv_workspace_bytes", "tv_status_string", "tv_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(tv.lib_path)
+    for name in header_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    assert tv.status_string(0) == "TV_OK"
+    assert tv.status_string(-1) == "TV_ERR_NULL_POINTER"
+    assert tv.status_string(8) == "TV_ST_BAD_BLOCK"
+    assert tv.version() >= 1
+
+
+FAKE = 0x10000  # a non-null, 256-byte aligned value; never dereferenced
+
+
+def test_host_validation_rejects_before_launch(lib):
+    L = lib
+    P = FAKE
+    # tree build
+    assert L.tv_tree_build(P, P, P, -1, 8, P, P, P, P, P, P, P, None) == -3
+    assert L.tv_tree_build(P, P, P, 1, 0, P, P, P, P, P, P, P, None) == -3
+    assert L.tv_tree_build(P, P, P, 1, 1025, P, P, P, P, P, P, P, None) == -3
+    assert L.tv_tree_build(None, P, P, 1, 8, P, P, P, P, P, P, P, None) == -1
+    assert L.tv_tree_build(None, None, None, 0, 8, None, None, None, None, None, None, None,
+                           None) == 0
+    # accept
+    assert L.tv_greedy_accept(P, P, P, P, P, 1, 8, -1, P, P, P, P, None) == -3
+    assert L.tv_greedy_accept(P, None, P, P, P, 1, 8, 4, P, P, P, P, None) == -1
+    # geometry checks
+    g = tv.geom(32, 8, 128)
+    bad_d = tv.geom(32, 8, 96)
+    bad_group = tv.geom(30, 8, 128)
+    bad_block = tv.geom(32, 8, 128, block_size=32)
+    bad_style = tv.geom(32, 8, 128, rope_style=2)
+    for bg in (bad_d, bad_group, bad_block, bad_style):
+        assert L.tv_kv_commit(ctypes.byref(bg), 1, P, P, 4, P, P, P, 8, P, P, 10, P, P, P, P,
+                              None) == -2
+    assert L.tv_kv_commit(ctypes.byref(g), 1, P, P, 4, P, None, P, 8, P, P, 10, P, P, P, P,
+                          None) == -1
+    assert L.tv_kv_commit(ctypes.byref(g), 0, None, None, 4, None, None, None, 8, None, None, 10,
+                          None, None, None, None, None) == 0
+    # attention
+    args = [P, P, P, P, P, P, P, P, P, 8, P, P, 100, P, P, 1 << 20, P, None]
+    assert L.tv_tree_attention_verify(ctypes.byref(bad_d), 1, 41, *args) == -2
+    assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 0, *args) == -3
+    assert L.tv_tree_attention_verify(ctypes.byref(g), 0, 41, *args) == 0
+    nul = list(args)
+    nul[0] = None
+    assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 41, *nul) == -1
+    mis = list(args)
+    mis[0] = FAKE + 2
+    assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 41, *mis) == -5
+    mis = list(args)
+    mis[14] = FAKE + 16                                   # workspace needs 256-byte alignment
+    assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 41, *mis) == -5
+    assert L.tv_workspace_bytes(ctypes.byref(bad_d), 1, 41, ctypes.byref(ctypes.c_size_t())) == -2
+    assert L.tv_workspace_bytes(ctypes.byref(g), 1, 41, None) == -1
