@@ -14,12 +14,11 @@ int launch_attention_mma(const tv_geom* geom, int batch, int max_nodes, const vo
                          size_t ws_bytes, int32_t* status, cudaStream_t stream);
 
 static int check_device() {
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TV_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return TV_ERR_CUDA;
-  return (major == 10 && minor == 3) ? TV_OK : TV_ERR_DEVICE;
+  const int dev = current_device();
+  if (dev < 0) return TV_ERR_CUDA;
+  const int ok = device_is_sm103(dev);
+  if (ok < 0) return TV_ERR_CUDA;
+  return ok ? TV_OK : TV_ERR_DEVICE;
 }
 }  // namespace tv
 

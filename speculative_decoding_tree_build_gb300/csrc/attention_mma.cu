@@ -465,10 +465,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) attn_mma_kernel(const __grid_c
 namespace tv {
 
 int mma_grid() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  return sms;
+  const int dev = current_device();
+  return dev < 0 ? -1 : device_sm_count(dev);
 }
 
 size_t mma_workspace_bytes(int batch, int hkv, int group, int max_nodes, int head_dim, int grid) {
@@ -528,17 +526,16 @@ int launch_attention_mma(const tv_geom* geom, int batch, int max_nodes, const vo
   const size_t smem_fixed = D == 128 ? MmaCfg<128>::kFixed : MmaCfg<64>::kFixed;
   const size_t smem = smem_fixed + static_cast<size_t>(batch + 1) * sizeof(long long);
   if (smem > 227 * 1024) return TV_ERR_BAD_SIZE;
-  cudaError_t err;
+  static size_t smem_set128[kMaxDevices] = {0}, smem_set64[kMaxDevices] = {0};
+  const int dev = current_device();
+  if (dev < 0) return TV_ERR_CUDA;
   if (D == 128) {
-    err = cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err == cudaSuccess) attn_mma_kernel<128><<<grid, kMmaThreads, smem, stream>>>(p);
+    if (!ensure_smem(attn_mma_kernel<128>, smem, smem_set128, dev)) return TV_ERR_CUDA;
+    attn_mma_kernel<128><<<grid, kMmaThreads, smem, stream>>>(p);
   } else {
-    err = cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err == cudaSuccess) attn_mma_kernel<64><<<grid, kMmaThreads, smem, stream>>>(p);
+    if (!ensure_smem(attn_mma_kernel<64>, smem, smem_set64, dev)) return TV_ERR_CUDA;
+    attn_mma_kernel<64><<<grid, kMmaThreads, smem, stream>>>(p);
   }
-  if (err != cudaSuccess) return TV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -37,7 +37,8 @@ kv_commit_kernel(const int32_t* __restrict__ accept_path, const int32_t* __restr
   if (status[b] != 0) return;
   const int a = accept_len[b];
   const int plen = prompt_len[b];
-  if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0) {
+  const int held0 = n_blocks[b];
+  if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0 || held0 < 0 || held0 > max_blocks) {
     if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
     return;
   }
@@ -141,13 +142,10 @@ extern "C" int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* a
       !v_cache || !new_len || !released || !released_count || !status)
     return TV_ERR_NULL_POINTER;
   if (!tv::aligned(k_cache, 16) || !tv::aligned(v_cache, 16)) return TV_ERR_MISALIGNED;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(tv::kv_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tv::kCommitSmem) != cudaSuccess)
-      return TV_ERR_CUDA;
-    configured = true;
-  }
+  static size_t smem_set[tv::kMaxDevices] = {0};
+  const int dev = tv::current_device();
+  if (dev < 0) return TV_ERR_CUDA;
+  if (!tv::ensure_smem(tv::kv_commit_kernel, tv::kCommitSmem, smem_set, dev)) return TV_ERR_CUDA;
   const int head_vecs = geom->head_dim / 8;
   tv::kv_commit_kernel<<<batch, tv::kCommitThreads, tv::kCommitSmem, tv::as_stream(stream)>>>(
       accept_path, accept_len, max_depth, prompt_len, block_table, n_blocks, max_blocks_per_req,

@@ -19,6 +19,50 @@ inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
+// Per-device facts queried once (benign race: every writer stores the same value).
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+inline int device_sm_count(int dev) {
+  static int cache[kMaxDevices] = {0};
+  if (cache[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = sms;
+  }
+  return cache[dev];
+}
+
+// 1 when the device is sm_103 (GB300), 0 otherwise, -1 on error
+inline int device_is_sm103(int dev) {
+  static int cache[kMaxDevices] = {0};   // 0 unknown, 1 yes, 2 no
+  if (cache[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return -1;
+    cache[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cache[dev] == 1 ? 1 : 0;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (and again
+// only if a larger size is needed).
+template <typename Kernel>
+inline bool ensure_smem(Kernel k, size_t bytes, size_t* done_per_device, int dev) {
+  if (done_per_device[dev] >= bytes) return true;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  done_per_device[dev] = bytes;
+  return true;
+}
+
 inline int check_geom(const tv_geom* g) {
   if (g == nullptr) return TV_ERR_NULL_POINTER;
   if (g->head_dim != 64 && g->head_dim != 128) return TV_ERR_BAD_GEOMETRY;
