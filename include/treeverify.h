@@ -157,6 +157,38 @@ int tv_tree_attention_verify(const tv_geom* geom, int32_t batch, int32_t max_nod
                              size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * Allocation-free variant of tv_tree_attention_verify. The paper has no
+ * counterpart to this call: it exists for callers that cannot obtain device
+ * memory - a plugin inside a host framework that only receives a stream and
+ * tensors, code running while another component owns the whole device memory
+ * pool, or a latency-critical loop that must not call cudaMalloc (which can
+ * synchronise the device). Same arguments and results as
+ * tv_tree_attention_verify, without the workspace.
+ *
+ *  - Scratch comes from a static device array of TV_NOALLOC_SCRATCH_BYTES
+ *    (64 MiB) inside the library. The runtime reserves it on a GPU the first
+ *    time this call runs there and keeps it until the process exits.
+ *  - The first call on each device looks up that array's device address (with
+ *    the device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and clears the part that
+ *    must start at zero itself. Calls that overlap on the GPU (other streams,
+ *    other threads) race on it: serialise them.
+ *  - A batch or tree that needs more scratch than TV_NOALLOC_SCRATCH_BYTES
+ *    (see tv_workspace_bytes) is rejected with TV_ERR_WORKSPACE and nothing
+ *    is launched.
+ *  - Calls no cudaMalloc/cudaFree or any allocating routine.
+ */
+#define TV_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int tv_tree_attention_verify_noalloc(const tv_geom* geom, int32_t batch, int32_t max_nodes,
+                                     const void* q, const void* k_new, const void* v_new,
+                                     const int32_t* cu_nodes, const int32_t* positions,
+                                     const uint32_t* mask_bits, const int32_t* prompt_len,
+                                     const int32_t* block_table, const int32_t* n_blocks,
+                                     int32_t max_blocks_per_req, void* k_cache, void* v_cache,
+                                     int32_t num_blocks, void* out, int32_t* status,
+                                     void* stream);
+
+/*
  * Greedy acceptance walk ([ATLAS] §4: from the root, move to the child whose
  * token equals the target's choice, stop at the first miss, the target's
  * token there is the correction / bonus; [GLOSSARY] three-part experiment

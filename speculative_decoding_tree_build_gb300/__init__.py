@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
-    "tree_build", "tree_attention_verify", "greedy_accept", "kv_commit", "status_string",
+    "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit", "status_string",
     "version",
 ]
 
@@ -51,6 +51,8 @@ _SIGS = {
     "tv_tree_build": [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P],
     "tv_tree_attention_verify": [ctypes.POINTER(TvGeom), _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                  _P, _P, _I, _P, _P, _I, _P, _P, _SZ, _P, _P],
+    "tv_tree_attention_verify_noalloc": [ctypes.POINTER(TvGeom), _I, _I, _P, _P, _P, _P, _P,
+                                         _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P],
     "tv_greedy_accept": [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P],
     "tv_kv_commit": [ctypes.POINTER(TvGeom), _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
                      _P, _P, _P, _P],
@@ -152,6 +154,22 @@ def tree_attention_verify(g: TvGeom, max_nodes, q, k_new, v_new, cu_nodes, posit
         _ptr(n_blocks, I32), block_table.shape[1], _ptr(k_cache, BF16, "k_cache"),
         _ptr(v_cache, BF16, "v_cache"), k_cache.shape[0], _ptr(out, BF16, "out"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(status, I32), _stream(stream)))
+
+
+def tree_attention_verify_noalloc(g: TvGeom, max_nodes, q, k_new, v_new, cu_nodes, positions,
+                                  mask_bits, prompt_len, block_table, n_blocks, k_cache, v_cache,
+                                  out, status, stream=None):
+    """tree_attention_verify without a workspace, for callers that cannot
+    allocate device memory: scratch comes from a fixed-size array inside the
+    library (see include/treeverify.h for its limits and sharing rules)."""
+    batch = cu_nodes.numel() - 1
+    return _check("tv_tree_attention_verify_noalloc", load().tv_tree_attention_verify_noalloc(
+        ctypes.byref(g), batch, max_nodes, _ptr(q, BF16, "q"), _ptr(k_new, BF16, "k_new"),
+        _ptr(v_new, BF16, "v_new"), _ptr(cu_nodes, I32), _ptr(positions, I32),
+        _ptr(mask_bits, None), _ptr(prompt_len, I32), _ptr(block_table, I32, "block_table"),
+        _ptr(n_blocks, I32), block_table.shape[1], _ptr(k_cache, BF16, "k_cache"),
+        _ptr(v_cache, BF16, "v_cache"), k_cache.shape[0], _ptr(out, BF16, "out"),
         _ptr(status, I32), _stream(stream)))
 
 

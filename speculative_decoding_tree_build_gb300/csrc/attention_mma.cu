@@ -469,6 +469,12 @@ int mma_grid() {
   return dev < 0 ? -1 : device_sm_count(dev);
 }
 
+// Bytes at the start of the workspace that must be zero before a call (the
+// per-unit arrival counters).
+size_t mma_counter_bytes(int batch, int hkv, int group, int max_nodes) {
+  return ws_counter_bytes(batch, hkv, (group * max_nodes + kMmaRows - 1) / kMmaRows);
+}
+
 size_t mma_workspace_bytes(int batch, int hkv, int group, int max_nodes, int head_dim, int grid) {
   const int nrg_max = (group * max_nodes + kMmaRows - 1) / kMmaRows;
   return ws_counter_bytes(batch, hkv, nrg_max) +
