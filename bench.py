@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "tree-verify tokens/s at 1 GB300; attention HBM GB/s & % roofline per step"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
-ATTN_SOURCES = ("attention_mma.cu", "tv_plan.cuh", "tv_common.cuh")
+ATTN_SOURCES = ("attention_tc.cu", "tv_sm100.cuh", "tv_common.cuh")
 
 
 def parse():

@@ -70,7 +70,7 @@ extern "C" {
 #define TV_ST_BAD_PARENT 4         /* parent[i] outside [0, i-1] for some i >= 1 */
 #define TV_ST_BAD_BLOCK 8          /* a needed block-table entry is missing or out of range */
 #define TV_ST_PATH_OVERFLOW 16     /* accepted path longer than max_depth */
-#define TV_ST_TIMEOUT 32           /* a bounded device wait gave up (workspace must be re-zeroed) */
+#define TV_ST_TIMEOUT 32           /* a bounded device wait gave up; that request's outputs are invalid */
 
 #define TV_MAX_NODES 1024          /* largest tree (root included) per request */
 #define TV_BLOCK_SIZE 16
@@ -87,10 +87,10 @@ typedef struct tv_geom {
 
 /*
  * Workspace size for tv_tree_attention_verify on the CURRENT device.
- * The workspace holds split-KV partial results and per-unit arrival
- * counters. It must be zero-filled once before its first use; every call
- * that finishes without TV_ST_TIMEOUT leaves it zero-filled again, so it can
- * be reused by later calls on the same stream without clearing.
+ * The workspace holds the rotated queries, split-KV partial results and
+ * merge records of one call. Its contents need no initialisation (every call
+ * writes what it reads); calls that overlap on the GPU must use different
+ * workspaces.
  * Returns TV_OK and writes *bytes, or a TV_ERR_* code.
  */
 int tv_workspace_bytes(const tv_geom* geom, int32_t batch, int32_t max_nodes, size_t* bytes);
@@ -141,7 +141,7 @@ int tv_tree_build(const int32_t* parents, const int32_t* cu_nodes, const int32_t
  *                 rotated k_new and the raw v_new of node i at slot P_b + i.
  *                 Every block covering slots [0, P_b + N_b) must be held.
  *  out            bf16 [T][Hq][D] out  attention output per node and query head
- *  workspace      device scratch of tv_workspace_bytes() bytes (zeroed once)
+ *  workspace      device scratch of tv_workspace_bytes() bytes (256-byte aligned)
  *  status         int32 [batch] in/out requests whose status carries a tree
  *                 flag are skipped; TV_ST_BAD_BLOCK / TV_ST_TIMEOUT are OR-ed in.
  * Rotated K is rounded to bf16 (round-to-nearest-even) after an fp32
@@ -170,9 +170,10 @@ int tv_tree_attention_verify(const tv_geom* geom, int32_t batch, int32_t max_nod
  *    time this call runs there and keeps it until the process exits.
  *  - The first call on each device looks up that array's device address (with
  *    the device current); make that first call before any stream capture.
- *  - Every call on a device shares the one array and clears the part that
- *    must start at zero itself. Calls that overlap on the GPU (other streams,
- *    other threads) race on it: serialise them.
+ *  - Every call on a device shares the one array (nothing in it needs to
+ *    start at zero: a call writes each record before reading it). Calls that
+ *    overlap on the GPU (other streams, other threads) race on it: serialise
+ *    them.
  *  - A batch or tree that needs more scratch than TV_NOALLOC_SCRATCH_BYTES
  *    (see tv_workspace_bytes) is rejected with TV_ERR_WORKSPACE and nothing
  *    is launched.

@@ -1,17 +1,17 @@
 // C entry points of libtreeverify that are not tied to one kernel file:
-// workspace sizing, the attention entry point's argument checks and
-// dispatch, status names and the interface version.
-#include "tv_plan.cuh"
+// workspace sizing, the attention entry point's argument checks and launch,
+// status names and the interface version.
+#include "tv_common.cuh"
 
 namespace tv {
-size_t mma_workspace_bytes(int batch, int hkv, int group, int max_nodes, int head_dim, int grid);
-int mma_grid();
-int launch_attention_mma(const tv_geom* geom, int batch, int max_nodes, const void* q,
-                         const void* k_new, const void* v_new, const int32_t* cu_nodes,
-                         const int32_t* positions, const uint32_t* mask, const int32_t* prompt_len,
-                         const int32_t* block_table, const int32_t* n_blocks, int max_blocks,
-                         void* k_cache, void* v_cache, int num_blocks, void* out, void* workspace,
-                         size_t ws_bytes, int32_t* status, cudaStream_t stream);
+size_t tc_workspace_bytes(int batch, int hq, int hkv, int max_nodes, int head_dim, int grid);
+int tc_grid();
+int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const void* q,
+                        const void* k_new, const void* v_new, const int32_t* cu_nodes,
+                        const int32_t* positions, const uint32_t* mask, const int32_t* prompt_len,
+                        const int32_t* block_table, const int32_t* n_blocks, int max_blocks,
+                        void* k_cache, void* v_cache, int num_blocks, void* out, void* workspace,
+                        size_t ws_bytes, int32_t* status, cudaStream_t stream);
 
 static int check_device() {
   const int dev = current_device();
@@ -30,11 +30,10 @@ extern "C" int tv_workspace_bytes(const tv_geom* geom, int32_t batch, int32_t ma
   if (rc != TV_OK) return rc;
   if (bytes == nullptr) return TV_ERR_NULL_POINTER;
   if (batch < 0 || max_nodes < 1 || max_nodes > TV_MAX_NODES) return TV_ERR_BAD_SIZE;
-  const int grid = tv::mma_grid();
+  const int grid = tv::tc_grid();
   if (grid <= 0) return TV_ERR_CUDA;
-  *bytes = tv::mma_workspace_bytes(batch, geom->num_kv_heads,
-                                   geom->num_q_heads / geom->num_kv_heads, max_nodes,
-                                   geom->head_dim, grid);
+  *bytes = tv::tc_workspace_bytes(batch, geom->num_q_heads, geom->num_kv_heads, max_nodes,
+                                  geom->head_dim, grid);
   return TV_OK;
 }
 
@@ -61,10 +60,10 @@ extern "C" int tv_tree_attention_verify(const tv_geom* geom, int32_t batch, int3
     return TV_ERR_MISALIGNED;
   rc = tv::check_device();
   if (rc != TV_OK) return rc;
-  return tv::launch_attention_mma(geom, batch, max_nodes, q, k_new, v_new, cu_nodes, positions,
-                                  mask_bits, prompt_len, block_table, n_blocks, max_blocks_per_req,
-                                  k_cache, v_cache, num_blocks, out, workspace, workspace_bytes,
-                                  status, tv::as_stream(stream));
+  return tv::launch_attention_tc(geom, batch, max_nodes, q, k_new, v_new, cu_nodes, positions,
+                                 mask_bits, prompt_len, block_table, n_blocks, max_blocks_per_req,
+                                 k_cache, v_cache, num_blocks, out, workspace, workspace_bytes,
+                                 status, tv::as_stream(stream));
 }
 
 extern "C" const char* tv_status_string(int code) {

@@ -13,11 +13,10 @@
 // translation unit's module, which the CUDA runtime loads (and so reserves the
 // array) the first time the entry point is used on a device; it stays reserved
 // until the process exits. The paper has no counterpart to this call.
-#include "tv_plan.cuh"
+#include "tv_common.cuh"
 
 namespace tv {
 
-size_t mma_counter_bytes(int batch, int hkv, int group, int max_nodes);
 
 constexpr size_t kTvNoAllocScratchBytes = TV_NOALLOC_SCRATCH_BYTES;
 
@@ -60,11 +59,8 @@ extern "C" int tv_tree_attention_verify_noalloc(
   void* scratch = nullptr;
   rc = tv::scratch_for_current_device(&scratch);
   if (rc != TV_OK) return rc;
-  // The array keeps whatever the previous call left; the arrival counters
-  // must start at zero.
-  const int group = geom->num_q_heads / geom->num_kv_heads;
-  const size_t zero = tv::mma_counter_bytes(batch, geom->num_kv_heads, group, max_nodes);
-  if (cudaMemsetAsync(scratch, 0, zero, tv::as_stream(stream)) != cudaSuccess) return TV_ERR_CUDA;
+  // The array keeps whatever the previous call left. Nothing in it has to
+  // start at zero: every call writes each scratch record before reading it.
   return tv_tree_attention_verify(geom, batch, max_nodes, q, k_new, v_new, cu_nodes, positions,
                                   mask_bits, prompt_len, block_table, n_blocks,
                                   max_blocks_per_req, k_cache, v_cache, num_blocks, out, scratch,
