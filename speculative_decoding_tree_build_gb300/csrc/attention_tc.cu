@@ -18,11 +18,12 @@
 //     page so every row a tile reads is finite.
 //  2. attn_tc_kernel: keys are cache slots [0, P + N); slots >= P are tested
 //     against the node's ancestor bit row. One CTA per SM, warp-specialised:
-//       warp 0      TMA producer: Q tiles and 16-row KV pages (4-D tensor
+//       warp 0      TMA producer: Q tiles and 16-row K pages (4-D tensor
 //                   maps over the paged pools, 128-byte swizzle)
 //       warp 1      MMA issuer: S = Q K^T (A, B in shared memory) and
 //                   O += P V (P read from Tensor Memory), fp32 accumulators
-//       warps 2-9   two 128-thread softmax groups, one Tensor Memory lane
+//       warp 2      TMA producer for V (K and V are released separately)
+//       warps 3-10  two 128-thread softmax groups, one Tensor Memory lane
 //                   (= one query row) per thread, ping-ponging two 128-row
 //                   M tiles so the tensor core always has work.
 //     Query rows of a unit are (node, query head in the GQA group), node
@@ -43,7 +44,7 @@ namespace tv {
 
 constexpr int kTcBN = 128;          // keys per tile
 constexpr int kTcStages = 2;        // K/V pipeline depth
-constexpr int kTcThreads = 320;     // 10 warps
+constexpr int kTcThreads = 352;     // 11 warps
 constexpr int kTcMaxBatch = 4096;
 constexpr int kRopeNodes = 4;       // nodes per pre-pass CTA
 constexpr int kRopeBatch = 4;       // loads in flight per pre-pass thread
@@ -94,6 +95,7 @@ template <int D>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_constant__ RopeParams p) {
   constexpr int D2 = D / 2;
   __shared__ float2 s_cs[kRopeNodes][D2];
+  __shared__ int s_blk[kRopeNodes];      // cache block of each node's tentative slot
   grid_launch_dependents();              // the attention grid may start its prologue
   const int b = blockIdx.y;
   const int t0 = p.cu_nodes[b];
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
     return;
   }
+  if (threadIdx.x < i1 - i0) s_blk[threadIdx.x] = trow[(plen + i0 + threadIdx.x) / TV_BLOCK_SIZE];
   for (int idx = threadIdx.x; idx < (i1 - i0) * D2; idx += blockDim.x) {
     const int nd = idx / D2, pr = idx % D2;
     float sn, cs;
@@ -178,8 +181,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
         const int slot = plen + i;
         dst = reinterpret_cast<uint4*>(
             (isv ? p.v_cache : p.k_cache) +
-            ((static_cast<size_t>(trow[slot / TV_BLOCK_SIZE]) * p.hkv + hh) * TV_BLOCK_SIZE +
-             slot % TV_BLOCK_SIZE) * D);
+            ((static_cast<size_t>(s_blk[nd]) * p.hkv + hh) * TV_BLOCK_SIZE + slot % TV_BLOCK_SIZE) * D);
         if (isv) {                                              // value: plain copy
           dst[v] = xa[u];
           if (!style0) dst[v + VPH / 2] = xb[u];
@@ -381,7 +383,7 @@ struct TcCfg {
 
 struct TcBars {
   uint64_t q_full, q_empty, drain;
-  uint64_t k_full[kTcStages], v_full[kTcStages], kv_empty[kTcStages];
+  uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
   uint64_t s_ready[2], p_ready[2], o_done[2], o_free[2];
 };
 
@@ -409,7 +411,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(&bars.s_ready[m], 1);
@@ -440,16 +443,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int G = p.group, npm = p.npm;
   const int32_t* table_base = p.block_table;
 
-  if (warp == 0) {
-    // ================================================= TMA producer
-    // The whole warp runs this loop: lane j fetches page j's block-table
-    // entry (one coalesced load per tile) and issues that page's copies.
-    {
-      uint32_t it = 0, qs = 0;
-      bool ok = true;
-      for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
-           g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
-        if (g.skip) continue;
+  if (warp == 0 || warp == 2) {
+    // ================================================= TMA producers
+    // warp 0 streams Q and K, warp 2 streams V. K of a stage is free once the
+    // S MMAs that read it finished, V once the PV MMAs did, so the two
+    // streams run ahead independently. The whole warp runs the loop: lane j
+    // fetches page j's block-table entry (one coalesced load per tile) and
+    // issues that page's copies.
+    const bool is_k = warp == 0;
+    uint64_t* full = is_k ? bars.k_full : bars.v_full;
+    uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+    uint8_t* dst_base = is_k ? sK : sV;
+    const CUtensorMap* map = is_k ? &p.kmap : &p.vmap;
+    uint32_t it = 0, qs = 0;
+    bool ok = true;
+    for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
+         g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
+      if (g.skip) continue;
+      if (is_k) {
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
         if (!ok) break;
         ++qs;
@@ -461,68 +472,72 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
               tma_load_4d(sQ + (m * C::kHalves + h) * C::kHalfBytes, &p.qmap, h * 64, 0, g.kvh,
                           g.t0 + g.node0 + m * npm, &bars.q_full);
         }
-        const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
-        const long long end = static_cast<long long>(g.plen) + g.n;
-        for (int t = g.tile0; t < g.tile1; ++t, ++it) {
-          const int s = it % kTcStages;
-          const int p0 = t * (kTcBN / TV_BLOCK_SIZE);
-          const long long hi = min(end, static_cast<long long>(t + 1) * kTcBN);
-          const int np = static_cast<int>((hi + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE) - p0;
-          const int blk = lane < np ? __ldg(trow + p0 + lane) : 0;
-          ok = __shfl_sync(0xffffffffu,
-                           lane == 0 ? mbar_wait(&bars.kv_empty[s], ((it / kTcStages) & 1) ^ 1, abort) : false, 0);
-          if (!ok) break;
-          if (lane == 0) {
-            const uint32_t bytes = np * C::kHalves * 2048u;
-            mbar_arrive_expect_tx(&bars.k_full[s], bytes);
-            mbar_arrive_expect_tx(&bars.v_full[s], bytes);
-          }
-          __syncwarp();
-          if (lane < np) {
-            uint8_t* dk = sK + s * C::kTileBytes + lane * 2048;
-            uint8_t* dv = sV + s * C::kTileBytes + lane * 2048;
+      }
+      const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
+      const long long end = static_cast<long long>(g.plen) + g.n;
+      for (int t = g.tile0; t < g.tile1; ++t, ++it) {
+        const int s = it % kTcStages;
+        const int p0 = t * (kTcBN / TV_BLOCK_SIZE);
+        const long long hi = min(end, static_cast<long long>(t + 1) * kTcBN);
+        const int np = static_cast<int>((hi + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE) - p0;
+        const int blk = lane < np ? __ldg(trow + p0 + lane) : 0;
+        ok = __shfl_sync(0xffffffffu,
+                         lane == 0 ? mbar_wait(&empty[s], ((it / kTcStages) & 1) ^ 1, abort) : false, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], np * C::kHalves * 2048u);
+        __syncwarp();
+        if (lane < np) {
 #pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) {
-              tma_load_4d(dk + h * C::kHalfBytes, &p.kmap, h * 64, 0, g.kvh, blk, &bars.k_full[s]);
-              tma_load_4d(dv + h * C::kHalfBytes, &p.vmap, h * 64, 0, g.kvh, blk, &bars.v_full[s]);
-            }
-          }
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_4d(dst_base + s * C::kTileBytes + lane * 2048 + h * C::kHalfBytes, map, h * 64, 0,
+                        g.kvh, blk, &full[s]);
         }
       }
-      // never leave copies in flight: wait for the stages this warp filled
-      for (uint32_t k = (it > kTcStages ? it - kTcStages : 0); lane == 0 && k < it; ++k) {
-        const int s = k % kTcStages;
-        volatile int no_abort = 0;
-        mbar_wait(&bars.k_full[s], (k / kTcStages) & 1, &no_abort);
-        mbar_wait(&bars.v_full[s], (k / kTcStages) & 1, &no_abort);
-      }
+    }
+    // never leave copies in flight: wait for the stages this warp filled
+    for (uint32_t k = (it > kTcStages ? it - kTcStages : 0); lane == 0 && k < it; ++k) {
+      volatile int no_abort = 0;
+      mbar_wait(&full[k % kTcStages], (k / kTcStages) & 1, &no_abort);
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, kTcBN, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      // A single thread issues every MMA, so the issue path must be short:
+      // the shared-memory descriptors are built once here and each K step
+      // only adds a compile-time offset (the start-address field is the low
+      // 14 bits, in 16-byte units; stage bases are far below 256 KB, so the
+      // addition never carries out of the field).
+      const uint64_t dQ0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dQ1 = smem_desc_sw128(smem_u32(sQ) + C::kHalves * C::kHalfBytes, 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dK1 = smem_desc_sw128(smem_u32(sK) + C::kTileBytes, 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(smem_u32(sV), C::kHalfBytes, 1024);
+      const uint64_t dV1 = smem_desc_sw128(smem_u32(sV) + C::kTileBytes, C::kHalfBytes, 1024);
+      static_assert(kTcStages == 2, "descriptor bases are precomputed for two stages");
       uint32_t it = 0, qs = 0, pc[2] = {0, 0}, of[2] = {0, 0};
       bool used[2] = {false, false};
       bool ok = true;
       auto issue_s = [&](int m, int s) {
         const uint32_t d = tbase + m * 256;
+        const uint64_t a0 = m ? dQ1 : dQ0;
+        const uint64_t b0 = s ? dK1 : dK0;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * C::kHalfBytes + (k % 4) * 32;
-          const uint64_t a = smem_desc_sw128(sQa + m * C::kHalves * C::kHalfBytes + off, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(sKa + s * C::kTileBytes + off, 16, 1024);
-          mma_ss(d, a, bdesc, idS, k > 0 ? 1u : 0u);
+          constexpr uint32_t kStep = 32 / 16;                       // 32 bytes per K step
+          const uint64_t off = (k / 4) * (C::kHalfBytes / 16) + (k % 4) * kStep;
+          mma_ss(d, a0 + off, b0 + off, idS, k > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_ready[m]);
       };
       auto issue_pv = [&](int m, int s, int kchunks, bool accumulate) {
         const uint32_t d = tbase + m * 256 + 128;
         const uint32_t a = tbase + m * 256;
-        for (int k = 0; k < kchunks; ++k) {
-          const uint64_t bdesc = smem_desc_sw128(sVa + s * C::kTileBytes + k * 2048, C::kHalfBytes, 1024);
-          mma_ts(d, a + k * 8, bdesc, idO, (accumulate || k > 0) ? 1u : 0u);
+        const uint64_t b0 = s ? dV1 : dV0;
+#pragma unroll
+        for (int k = 0; k < kTcBN / 16; ++k) {
+          if (k < kchunks) mma_ts(d, a + k * 8, b0 + k * (2048 / 16), idO, (accumulate || k > 0) ? 1u : 0u);
         }
       };
       for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
@@ -534,40 +549,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         const int nt = g.tile1 - g.tile0;
         const long long end = static_cast<long long>(g.plen) + g.n;
         bool pv_started[2] = {false, false};
+        // Ping-pong order per step i: PV_0(i-1), S_0(i), PV_1(i-1), S_1(i).
+        // S_m(i) reuses the Tensor Memory columns P_m(i-1) occupies, so it is
+        // issued after PV_m(i-1); tcgen05 MMAs from one thread run in order.
+        // A PV never waits for the next K tile.
         for (int i = 0; i <= nt && ok; ++i) {
-          // i < nt: S of tile i (after the PV of tile i-1 that read the same
-          // Tensor Memory columns); i == nt: drain the last tile's PV
           const uint32_t iti = it + i;
           const int s = iti % kTcStages;
-          if (i < nt) {
-            if (!(ok = mbar_wait(&bars.k_full[s], (iti / kTcStages) & 1, abort))) break;
-            tc_fence_after();
-          }
           const int sp = (iti - 1) % kTcStages;
           int kch = 0;
           if (i > 0) {
             const long long hi = min(end, static_cast<long long>(g.tile0 + i) * kTcBN);
             kch = static_cast<int>((hi - static_cast<long long>(g.tile0 + i - 1) * kTcBN + 15) / 16);
-            if (!(ok = mbar_wait(&bars.v_full[sp], ((iti - 1) / kTcStages) & 1, abort))) break;
           }
           for (int m = 0; m < g.mt && ok; ++m) {
             if (i > 0) {
               if (!(ok = mbar_wait(&bars.p_ready[m], pc[m] & 1, abort))) break;
               ++pc[m];
-              tc_fence_after();
               if (!pv_started[m] && used[m]) {
                 if (!(ok = mbar_wait(&bars.o_free[m], of[m] & 1, abort))) break;
                 ++of[m];
-                tc_fence_after();
               }
+              if (m == 0 && !(ok = mbar_wait(&bars.v_full[sp], ((iti - 1) / kTcStages) & 1, abort))) break;
+              tc_fence_after();
               issue_pv(m, sp, kch, pv_started[m]);
               pv_started[m] = true;
               if (i == nt) mma_commit(&bars.o_done[m]);
             }
-            if (i < nt) issue_s(m, s);
+            if (i < nt) {
+              if (m == 0) {
+                if (!(ok = mbar_wait(&bars.k_full[s], (iti / kTcStages) & 1, abort))) break;
+                tc_fence_after();
+              }
+              issue_s(m, s);
+            }
           }
+          if (!ok) break;
+          if (i > 0) mma_commit(&bars.v_empty[sp]);
+          if (i < nt) mma_commit(&bars.k_empty[s]);
           if (i == nt - 1) mma_commit(&bars.q_empty);    // the last S of the segment
-          if (i > 0) mma_commit(&bars.kv_empty[sp]);
         }
         for (int m = 0; m < g.mt; ++m) used[m] = true;
         it += nt;
@@ -579,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
   } else {
     // ================================================= softmax groups
-    const int m = (warp - 2) >> 2;
+    const int m = (warp - 3) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + m * 256 + lane_addr;
@@ -753,8 +773,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 // partial (unnormalised O, reference max m, sum l, all per row) per
 // contributor. Merging is the usual log-sum-exp combination:
 //   out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,  M = max_c m_c.
-// Four CTAs per attention CTA, each 64 rows; every thread keeps
-// kMergeUnroll x contributors loads in flight.
+// kMergeSplit CTAs per split unit (32 rows each, 8 threads per row); each
+// thread loads kMergeChunk contributors' partials at once.
 
 struct MergeParams {
   const int32_t* tasks;
@@ -764,60 +784,79 @@ struct MergeParams {
 };
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeSplit = 4;      // CTAs per unit (64 rows each)
-constexpr int kMergeUnroll = 8;
+constexpr int kMergeSplit = 8;      // CTAs per unit (32 rows each)
+constexpr int kMergeChunk = 4;      // contributors whose loads are in flight together
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   grid_dependency_wait();            // the attention grid's partials and tasks are visible
-  const int c = blockIdx.x / kMergeSplit, quarter = blockIdx.x % kMergeSplit;
+  const int c = blockIdx.x / kMergeSplit, part_cta = blockIdx.x % kMergeSplit;
   const int32_t* rec = p.tasks + c * kTaskInts;
   if (rec[0] == 0) return;
-  const int b = rec[1], kvh = rec[2], node0 = rec[3], mt = rec[4], t0 = rec[5], n = rec[6];
+  const int kvh = rec[2], node0 = rec[3], mt = rec[4], t0 = rec[5], n = rec[6];
   const int c_first = rec[7], c_last = rec[8], first_slot = rec[9];
-  constexpr int kParts = kMergeThreads / 64;          // threads per row
+  constexpr int kRowsCta = 256 / kMergeSplit;         // 32 rows per CTA
+  constexpr int kParts = kMergeThreads / kRowsCta;    // 8 threads per row
   constexpr int kVecs = D / 4 / kParts;               // float4 per thread
-  const int r = quarter * 64 + (threadIdx.x & 63);
-  const int part = threadIdx.x >> 6;
+  const int r = part_cta * kRowsCta + threadIdx.x % kRowsCta;
+  const int part = threadIdx.x / kRowsCta;
   const int mm = r >> 7, rr = r & 127;
   const int G = p.group;
   const int nd = node0 + mm * p.npm + rr / G;
   if (mm >= mt || rr >= G * p.npm || nd >= n) return;
-  (void)b;
   const int nc = c_last - c_first + 1;
-  float mmax = -INFINITY;
-  for (int k = 0; k < nc; ++k) {
-    const int sl = k == 0 ? first_slot : 2 * (c_first + k);
-    const float* ml = p.partials + static_cast<size_t>(sl) * kSlotFloats(D) + D * 256;
-    mmax = fmaxf(mmax, __ldcg(ml + r));
-  }
-  float lsum = 0.f;
+  // single pass, online log-sum-exp over chunks of contributors
+  float m_run = -INFINITY, l_run = 0.f;
   float4 acc[kVecs];
 #pragma unroll
   for (int v = 0; v < kVecs; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < nc; ++k) {
-    const int sl = k == 0 ? first_slot : 2 * (c_first + k);
-    const float* base = p.partials + static_cast<size_t>(sl) * kSlotFloats(D);
-    const float mc = __ldcg(base + D * 256 + r);
-    if (mc == -INFINITY) continue;
-    const float w = fast_exp2(mc - mmax);
-    lsum += w * __ldcg(base + D * 256 + 256 + r);
-    const float4* o4 = reinterpret_cast<const float4*>(base);
+  for (int k0 = 0; k0 < nc; k0 += kMergeChunk) {
+    float mc[kMergeChunk], lc[kMergeChunk];
+    float4 x[kMergeChunk][kVecs];
 #pragma unroll
-    for (int v0 = 0; v0 < kVecs; v0 += kMergeUnroll) {
-      float4 x[kMergeUnroll];
+    for (int u = 0; u < kMergeChunk; ++u) {
+      const int k = k0 + u;
+      mc[u] = -INFINITY;
+      lc[u] = 0.f;
+      if (k < nc) {
+        const int sl = k == 0 ? first_slot : 2 * (c_first + k);
+        const float* base = p.partials + static_cast<size_t>(sl) * kSlotFloats(D);
+        mc[u] = __ldcg(base + D * 256 + r);
+        lc[u] = __ldcg(base + D * 256 + 256 + r);
+        const float4* o4 = reinterpret_cast<const float4*>(base);
 #pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) x[u] = __ldcg(o4 + (part * kVecs + v0 + u) * 256 + r);
-#pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
-        acc[v0 + u].x += w * x[u].x;
-        acc[v0 + u].y += w * x[u].y;
-        acc[v0 + u].z += w * x[u].z;
-        acc[v0 + u].w += w * x[u].w;
+        for (int v = 0; v < kVecs; ++v) x[u][v] = __ldcg(o4 + (part * kVecs + v) * 256 + r);
       }
     }
+    float m_new = m_run;
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) m_new = fmaxf(m_new, mc[u]);
+    if (m_new == -INFINITY) continue;
+    const float sc = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
+    l_run *= sc;
+#pragma unroll
+    for (int v = 0; v < kVecs; ++v) {
+      acc[v].x *= sc;
+      acc[v].y *= sc;
+      acc[v].z *= sc;
+      acc[v].w *= sc;
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) {
+      if (mc[u] == -INFINITY) continue;
+      const float w = fast_exp2(mc[u] - m_new);
+      l_run += w * lc[u];
+#pragma unroll
+      for (int v = 0; v < kVecs; ++v) {
+        acc[v].x += w * x[u][v].x;
+        acc[v].y += w * x[u][v].y;
+        acc[v].z += w * x[u][v].z;
+        acc[v].w += w * x[u][v].w;
+      }
+    }
+    m_run = m_new;
   }
-  const float inv = 1.f / lsum;
+  const float inv = 1.f / l_run;
   const int h = kvh * G + rr % G;
   uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(t0 + nd) * p.hq + h) * D +
                                         part * kVecs * 4);
