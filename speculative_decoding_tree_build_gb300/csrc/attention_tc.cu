@@ -10,7 +10,7 @@
 // attention" and its packed-vs-branch experiment; "02 · Token Tree 与 Tree
 // Attention" §3 (visible = prompt ∪ ancestors, RoPE at tree depth).
 //
-// Two launches on the caller's stream:
+// Three launches on the caller's stream:
 //  1. rope_append_kernel: rotates q (into the workspace) and k (into the
 //     tentative cache slots P + i, with the raw v) - "投机解码的树状注意力验证…",
 //     section "实现中的 KV Cache 与批处理约束": the tree's tentative KV is a
@@ -18,45 +18,51 @@
 //     page so every row a tile reads is finite.
 //  2. attn_tc_kernel: keys are cache slots [0, P + N); slots >= P are tested
 //     against the node's ancestor bit row. One CTA per SM, warp-specialised:
-//       warp 0      TMA producer: Q tiles and 16-row K pages (4-D tensor
-//                   maps over the paged pools, 128-byte swizzle)
-//       warp 1      MMA issuer: S = Q K^T (A, B in shared memory) and
-//                   O += P V (P read from Tensor Memory), fp32 accumulators
-//       warp 2      TMA producer for V (K and V are released separately)
-//       warps 3-10  two 128-thread softmax groups, one Tensor Memory lane
-//                   (= one query row) per thread, ping-ponging two 128-row
-//                   M tiles so the tensor core always has work.
+//       warp 0      TMA producer: Q tiles, then K and V 16-row pages (4-D
+//                   tensor maps over the paged pools, 128-byte swizzle)
+//       warp 2      idle (keeps the softmax warps on their lane quarters)
+//       warps 1, 3  MMA issuers, one per 128-row M tile: S = Q K^T (A, B in
+//                   shared memory) and O += P V (P read from Tensor Memory),
+//                   fp32 accumulators. Keys move in 64-key steps and each M
+//                   tile has two 64-column score buffers, so the tensor core
+//                   computes S(j + 1) while the softmax works on S(j).
+//       warps 4-11  two 128-thread softmax groups (one per M tile), one
+//                   Tensor Memory lane (= one query row) per thread.
 //     Query rows of a unit are (node, query head in the GQA group), node
-//     major, so one K/V tile feeds up to 256 rows. Work plan: a unit is
-//     (request, KV head, group of up to 256 rows); all units' key tiles are
-//     laid end to end and every CTA takes an equal contiguous share, computed
-//     on the device from cu_nodes/prompt_len (no host round trip), so each
-//     CTA moves the same amount of KV whatever the prompt-length mix.
+//     major, spread evenly over the eight 32-row quarters of the two M tiles,
+//     so one K/V tile feeds up to 256 rows. Work plan: a unit is (request,
+//     KV head, group of up to 256 rows); all units' key tiles are laid end to
+//     end and every CTA takes an equal contiguous share, computed on the
+//     device from cu_nodes/prompt_len (no host round trip), so each CTA moves
+//     the same amount of KV whatever the prompt-length mix.
 //  3. attn_merge_kernel: a unit cut between CTAs left one partial per CTA;
 //     this grid merges them (log-sum-exp), many CTAs and loads in flight.
 //  Launches 2 and 3 use programmatic dependent launch so their prologues
 //  overlap the previous grid's tail. No CTA ever waits for another CTA.
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "tv_sm100.cuh"
 
 namespace tv {
 
-constexpr int kTcBN = 128;          // keys per tile
-constexpr int kTcStages = 2;        // K/V pipeline depth
-constexpr int kTcThreads = 352;     // 11 warps
+constexpr int kTcBN = 128;          // keys per work-plan tile
+constexpr int kTcBK = 64;           // keys per pipeline step (S buffer width, K/V stage)
+constexpr int kTcStages = 4;        // K/V pipeline depth, in steps
+constexpr int kTcThreads = 384;     // 12 warps
+constexpr int kExpFmaEvery = 0;     // one exponential pair in this many on the FMA pipe (0: none)
 constexpr int kTcMaxBatch = 4096;
 constexpr int kRopeNodes = 4;       // nodes per pre-pass CTA
 constexpr int kRopeBatch = 4;       // loads in flight per pre-pass thread
 constexpr int kRopeThreads = 256;
 constexpr int kTaskInts = 16;       // merge-task record per attention CTA
 
-// floats of one partial-result slot: O [D/4 column blocks][256 rows] float4,
-// then the per-row reference max and sum
-__host__ __device__ constexpr size_t kSlotFloats(int d) { return static_cast<size_t>(256) * (d + 2); }
+// bytes of one partial-result slot: O / l as fp16 [D/8 column blocks][256
+// rows] x 16 B, then the per-row reference max and sum (fp32)
+__host__ __device__ constexpr size_t kSlotBytes(int d) { return static_cast<size_t>(256) * (2 * d + 8); }
 
 struct TcParams {
-  CUtensorMap qmap;      // rotated q in the workspace, dims (D, G, Hkv, T_cap)
+  CUtensorMap qmap;      // rotated q in the workspace, dims (D, G, Hkv, T_cap), box (64, G, 1, npq)
   CUtensorMap kmap;      // K pool, dims (D, 16, Hkv, num_blocks)
   CUtensorMap vmap;      // V pool
   const int32_t* cu_nodes;
@@ -66,9 +72,9 @@ struct TcParams {
   const int32_t* status;
   __nv_bfloat16* out;
   int32_t* tasks;        // kTaskInts per CTA: the split unit this CTA starts (merge work)
-  float* partials;       // two slots per CTA
+  uint8_t* partials;     // two slots of kSlotBytes(D) per CTA
   int32_t* status_rw;
-  int batch, max_nodes, t_cap, hq, hkv, group, npm, words, max_blocks, grid;
+  int batch, max_nodes, t_cap, hq, hkv, group, npq, words, max_blocks, grid;   // npq = 32 / G nodes per quarter
   float scale_log2;
 };
 
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
 // ------------------------------------------------------------ attention
 
 struct TcSeg {
-  int b, t0, n, plen, kvh, rg, node0, mt, tile0, tile1, ntiles;
+  int b, t0, n, plen, kvh, node0, nodes, mt, tile0, tile1, ntiles;
   bool whole, skip, valid;
   long long t_next, unit_t0;
   int my_slot;
@@ -248,17 +254,21 @@ struct TcShape {
   int t0, n, plen, nrg, tiles;
 };
 
+// Nodes per unit: two M tiles of four 32-lane quarters, 32 / G nodes each.
+__host__ __device__ __forceinline__ int tc_unit_nodes(int npq) { return 8 * npq; }
+
 __device__ __forceinline__ TcShape tc_shape(const TcParams& p, int b) {
   TcShape r;
   r.t0 = p.cu_nodes[b];
-  r.n = p.cu_nodes[b + 1] - r.t0;
+  const int t1 = p.cu_nodes[b + 1];
   r.plen = p.prompt_len[b];
+  r.n = t1 - r.t0;
   if (r.n < 1 || r.n > p.max_nodes || r.plen < 0 || r.t0 < 0 ||
       static_cast<long long>(r.t0) + r.n > p.t_cap) {
     r.nrg = r.tiles = 0;
     return r;
   }
-  r.nrg = (r.n + 2 * p.npm - 1) / (2 * p.npm);
+  r.nrg = (r.n + tc_unit_nodes(p.npq) - 1) / tc_unit_nodes(p.npq);
   r.tiles = static_cast<int>((static_cast<long long>(r.plen) + r.n + kTcBN - 1) / kTcBN);
   return r;
 }
@@ -328,18 +338,19 @@ __device__ TcSeg tc_segment(const TcParams& p, const int* s_pre, long long t, lo
     if (s_pre[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
+  const int st = p.status[b];            // loaded together with the request's shape
   const TcShape r = tc_shape(p, b);
   const long long local = t - s_pre[b];
   const int unit = static_cast<int>(local / r.tiles);
+  const int rg = unit % r.nrg;
   g.b = b;
   g.t0 = r.t0;
   g.n = r.n;
   g.plen = r.plen;
   g.kvh = unit / r.nrg;
-  g.rg = unit % r.nrg;
-  g.node0 = g.rg * 2 * p.npm;
-  const int nodes_u = min(2 * p.npm, r.n - g.node0);
-  g.mt = (nodes_u + p.npm - 1) / p.npm;
+  g.node0 = rg * tc_unit_nodes(p.npq);
+  g.nodes = min(tc_unit_nodes(p.npq), r.n - g.node0);
+  g.mt = (g.nodes + 4 * p.npq - 1) / (4 * p.npq);
   g.ntiles = r.tiles;
   g.tile0 = static_cast<int>(local % r.tiles);
   g.tile1 = static_cast<int>(min(static_cast<long long>(r.tiles), g.tile0 + (e - t)));
@@ -347,8 +358,32 @@ __device__ TcSeg tc_segment(const TcParams& p, const int* s_pre, long long t, lo
   g.whole = g.tile0 == 0 && g.tile1 == r.tiles;
   g.unit_t0 = s_pre[b] + static_cast<long long>(unit) * r.tiles;
   g.my_slot = 2 * blockIdx.x + (t == s ? 0 : 1);
-  g.skip = (p.status[b] & (TV_TREE_FLAGS | TV_ST_BAD_BLOCK)) != 0;
+  g.skip = (st & (TV_TREE_FLAGS | TV_ST_BAD_BLOCK)) != 0;
   return g;
+}
+
+// Query rows of a unit. An M tile is four 32-lane quarters (a warp may only
+// reach the Tensor Memory lanes of its own quarter, warp % 4). The unit's
+// nodes are spread in node order over the 4 * mt quarters as evenly as
+// possible, G rows per node (node major, query head minor), so the softmax
+// warps of all four SM sub-partitions get near-equal row counts.
+struct RowSplit {
+  int base, extra;   // quarter j holds base + (j < extra ? 1 : 0) nodes
+};
+
+__device__ __forceinline__ RowSplit row_split(int nodes, int mt) {
+  RowSplit r;
+  r.base = nodes / (4 * mt);
+  r.extra = nodes % (4 * mt);
+  return r;
+}
+
+__device__ __forceinline__ int quarter_first(const RowSplit& r, int j) {
+  return j * r.base + min(j, r.extra);
+}
+
+__device__ __forceinline__ int quarter_count(const RowSplit& r, int j) {
+  return r.base + (j < r.extra ? 1 : 0);
 }
 
 // 32 bits of visibility for key slots [k0, k0 + 32) of a row whose node has
@@ -372,20 +407,62 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t* mrow, int words
   return bits;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x on the FMA pipe, for a share of the softmax exponentials so that the
+// MUFU unit is not the only one working. Cody-Waite style reduction
+// x = j + f with j = rint(x) (adding 1.5 * 2^23 rounds x to an integer kept in
+// the low mantissa bits), 2^f for f in [-1/2, 1/2] by a cubic fitted for
+// minimax relative error (Lawson's reweighted least squares; 7.5e-5 at most,
+// far below the bf16 rounding P gets next), and 2^j added to the exponent
+// field. x is clamped at -125 so the exponent stays normal; 2^-125 vanishes
+// in every sum it enters (a fully masked row is discarded by its max).
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float q = fmaf(fmaf(fmaf(5.517166853e-02f, f, 2.426111251e-01f), f, 6.932609677e-01f), f,
+                       9.999280572e-01f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 template <int D>
 struct TcCfg {
-  static constexpr int kHalves = D / 64;
-  static constexpr uint32_t kHalfBytes = 128 * 128;                 // 128 rows x 128 B
-  static constexpr uint32_t kQBytes = 2 * kHalves * kHalfBytes;     // two M tiles
-  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;      // one K or V tile
-  static constexpr uint32_t kSmem = kQBytes + 2 * kTcStages * kTileBytes;
+  static constexpr int kHalves = D / 64;                            // 64-column halves of a row
+  static constexpr uint32_t kQHalfBytes = 128 * 128;                // Q: 128 rows x 128 B
+  static constexpr uint32_t kQBytes = 2 * kHalves * kQHalfBytes;    // two M tiles
+  static constexpr uint32_t kKvHalfBytes = kTcBK * 128;             // K/V stage: 64 keys x 128 B
+  static constexpr uint32_t kStageBytes = kHalves * kKvHalfBytes;   // one K or V stage
+  static constexpr uint32_t kSmem = kQBytes + 2 * kTcStages * kStageBytes;
 };
 
+// Arrival counts: the *_empty barriers take one arrival per MMA issuer (a
+// commit from an issuer with live rows, a plain arrive from one without);
+// p_ready and o_free one per softmax warp of the tile. s_ready / p_ready are
+// per (M tile, score buffer), so each has at most one phase outstanding.
+// kv_empty[s] completing also tells a softmax warp that both tiles' PV of
+// that step (the last MMAs to add to O before the next step) are done.
 struct TcBars {
-  uint64_t q_full, q_empty, drain;
-  uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
-  uint64_t s_ready[2], p_ready[2], o_done[2], o_free[2];
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+  uint64_t s_ready[2][2], p_ready[2][2], o_done[2], o_free[2], drain[2];
 };
+
+// 64-key steps of a segment (the last one may be partial)
+__device__ __forceinline__ int tc_steps(const TcSeg& g) {
+  const long long end = static_cast<long long>(g.plen) + g.n;
+  const long long hi = min(end, static_cast<long long>(g.tile1) * kTcBN);
+  return static_cast<int>((hi - static_cast<long long>(g.tile0) * kTcBN + kTcBK - 1) / kTcBK);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
@@ -395,8 +472,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::kQBytes;
-  uint8_t* sV = sK + kTcStages * C::kTileBytes;
-  int* s_pre = reinterpret_cast<int*>(sV + kTcStages * C::kTileBytes);
+  uint8_t* sV = sK + kTcStages * C::kStageBytes;
+  int* s_pre = reinterpret_cast<int*>(sV + kTcStages * C::kStageBytes);
   __shared__ TcBars bars;
   __shared__ int s_tmp[kTcThreads];
   __shared__ uint32_t s_tmem;
@@ -406,19 +483,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     s_abort = 0;
     mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 1);
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.q_empty, 2);
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
-      mbar_init(&bars.v_empty[s], 1);
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 2);
     }
     for (int m = 0; m < 2; ++m) {
-      mbar_init(&bars.s_ready[m], 1);
-      mbar_init(&bars.p_ready[m], 4);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars.s_ready[m][b], 1);
+        mbar_init(&bars.p_ready[m][b], 4);
+      }
       mbar_init(&bars.o_done[m], 1);
       mbar_init(&bars.o_free[m], 4);
+      mbar_init(&bars.drain[m], 1);
     }
     fence_mbar_init();
   }
@@ -440,227 +517,223 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const long long total = s_pre[p.batch];
   const long long cs = tc_cta_start(total, p.grid, blockIdx.x);
   const long long ce = tc_cta_start(total, p.grid, blockIdx.x + 1);
-  const int G = p.group, npm = p.npm;
+  const int G = p.group, npq = p.npq;
   const int32_t* table_base = p.block_table;
 
-  if (warp == 0 || warp == 2) {
-    // ================================================= TMA producers
-    // warp 0 streams Q and K, warp 2 streams V. K of a stage is free once the
-    // S MMAs that read it finished, V once the PV MMAs did, so the two
-    // streams run ahead independently. The whole warp runs the loop: lane j
-    // fetches page j's block-table entry (one coalesced load per tile) and
-    // issues that page's copies.
-    const bool is_k = warp == 0;
-    uint64_t* full = is_k ? bars.k_full : bars.v_full;
-    uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
-    uint8_t* dst_base = is_k ? sK : sV;
-    const CUtensorMap* map = is_k ? &p.kmap : &p.vmap;
-    uint32_t it = 0, qs = 0;
+  if (warp == 0) {
+    // ================================================= TMA producer
+    // Streams Q per segment and K + V per 64-key step (four 16-row pages of
+    // each) into one stage with one barrier: the issuer then waits once per
+    // step, and the stage is free once both tiles' PV MMAs (the last readers)
+    // finished. The whole warp runs the loop: lane j fetches page j's
+    // block-table entry and issues that page's copies.
+    uint32_t hc = 0, qs = 0;
     bool ok = true;
     for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
          g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
       if (g.skip) continue;
-      if (is_k) {
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
-        if (!ok) break;
-        ++qs;
-        if (lane == 0) {
-          const uint32_t qbox = 64u * 2u * G * npm;
-          mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * g.mt);
-          for (int m = 0; m < g.mt; ++m)
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(sQ + (m * C::kHalves + h) * C::kHalfBytes, &p.qmap, h * 64, 0, g.kvh,
-                          g.t0 + g.node0 + m * npm, &bars.q_full);
-        }
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
+      if (!ok) break;
+      ++qs;
+      if (lane == 0) {
+        // one box of npq nodes x G heads (<= 32 rows) per quarter and half;
+        // quarters without nodes are not loaded
+        const RowSplit rs = row_split(g.nodes, g.mt);
+        const uint32_t qbox = 64u * 2u * G * npq;
+        const int nq = min(4 * g.mt, g.nodes);
+        mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * nq);
+        for (int j = 0; j < nq; ++j)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_4d(sQ + ((j >> 2) * C::kHalves + h) * C::kQHalfBytes + (j & 3) * 4096, &p.qmap,
+                        h * 64, 0, g.kvh, g.t0 + g.node0 + quarter_first(rs, j), &bars.q_full);
       }
       const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
       const long long end = static_cast<long long>(g.plen) + g.n;
-      for (int t = g.tile0; t < g.tile1; ++t, ++it) {
-        const int s = it % kTcStages;
-        const int p0 = t * (kTcBN / TV_BLOCK_SIZE);
-        const long long hi = min(end, static_cast<long long>(t + 1) * kTcBN);
-        const int np = static_cast<int>((hi + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE) - p0;
-        const int blk = lane < np ? __ldg(trow + p0 + lane) : 0;
+      const int nh = tc_steps(g);
+      for (int j = 0; j < nh; ++j, ++hc) {
+        const int s = hc % kTcStages;
+        const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
+        const int np = static_cast<int>((min(end, k0 + kTcBK) - k0 + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
+        const int blk = lane < np ? __ldg(trow + k0 / TV_BLOCK_SIZE + lane) : 0;
         ok = __shfl_sync(0xffffffffu,
-                         lane == 0 ? mbar_wait(&empty[s], ((it / kTcStages) & 1) ^ 1, abort) : false, 0);
+                         lane == 0 ? mbar_wait(&bars.kv_empty[s], ((hc / kTcStages) & 1) ^ 1, abort) : false, 0);
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], np * C::kHalves * 2048u);
+        if (lane == 0) mbar_arrive_expect_tx(&bars.kv_full[s], np * C::kHalves * 2u * 2048u);
         __syncwarp();
         if (lane < np) {
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_4d(dst_base + s * C::kTileBytes + lane * 2048 + h * C::kHalfBytes, map, h * 64, 0,
-                        g.kvh, blk, &full[s]);
+          for (int h = 0; h < C::kHalves; ++h) {
+            tma_load_4d(sK + s * C::kStageBytes + h * C::kKvHalfBytes + lane * 2048, &p.kmap, h * 64, 0,
+                        g.kvh, blk, &bars.kv_full[s]);
+            tma_load_4d(sV + s * C::kStageBytes + h * C::kKvHalfBytes + lane * 2048, &p.vmap, h * 64, 0,
+                        g.kvh, blk, &bars.kv_full[s]);
+          }
         }
       }
     }
     // never leave copies in flight: wait for the stages this warp filled
-    for (uint32_t k = (it > kTcStages ? it - kTcStages : 0); lane == 0 && k < it; ++k) {
+    for (uint32_t k = (hc > kTcStages ? hc - kTcStages : 0); lane == 0 && k < hc; ++k) {
       volatile int no_abort = 0;
-      mbar_wait(&full[k % kTcStages], (k / kTcStages) & 1, &no_abort);
+      mbar_wait(&bars.kv_full[k % kTcStages], (k / kTcStages) & 1, &no_abort);
     }
-  } else if (warp == 1) {
-    // ================================================= MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ================================================= MMA issuers
+    // Warp 1 issues every MMA of M tile 0, warp 3 of M tile 1 (a thread needs
+    // about 60 cycles per tcgen05.mma; two issuers keep one tile's waits off
+    // the other's path). Each tile has two 64-key score buffers, so S(j + 1)
+    // is computed while the softmax works on S(j); the order per tile is
+    //   S(0), S(1), PV(0), S(2), PV(1), S(3), ...
+    // MMAs of one thread run in order, which is what lets S(j + 2) reuse the
+    // buffer P(j) occupies once PV(j) is issued. An issuer without rows in a
+    // segment still takes part in the stage hand-off with plain arrivals.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, kTcBN, false);
+      const int m = warp >> 1;
+      constexpr uint32_t idS = idesc_bf16_f32(128, kTcBK, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
-      // A single thread issues every MMA, so the issue path must be short:
-      // the shared-memory descriptors are built once here and each K step
-      // only adds a compile-time offset (the start-address field is the low
-      // 14 bits, in 16-byte units; stage bases are far below 256 KB, so the
-      // addition never carries out of the field).
-      const uint64_t dQ0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dQ1 = smem_desc_sw128(smem_u32(sQ) + C::kHalves * C::kHalfBytes, 16, 1024);
-      const uint64_t dK0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dK1 = smem_desc_sw128(smem_u32(sK) + C::kTileBytes, 16, 1024);
-      const uint64_t dV0 = smem_desc_sw128(smem_u32(sV), C::kHalfBytes, 1024);
-      const uint64_t dV1 = smem_desc_sw128(smem_u32(sV) + C::kTileBytes, C::kHalfBytes, 1024);
-      static_assert(kTcStages == 2, "descriptor bases are precomputed for two stages");
-      uint32_t it = 0, qs = 0, pc[2] = {0, 0}, of[2] = {0, 0};
-      bool used[2] = {false, false};
-      bool ok = true;
-      auto issue_s = [&](int m, int s) {
-        const uint32_t d = tbase + m * 256;
-        const uint64_t a0 = m ? dQ1 : dQ0;
-        const uint64_t b0 = s ? dK1 : dK0;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          constexpr uint32_t kStep = 32 / 16;                       // 32 bytes per K step
-          const uint64_t off = (k / 4) * (C::kHalfBytes / 16) + (k % 4) * kStep;
-          mma_ss(d, a0 + off, b0 + off, idS, k > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars.s_ready[m]);
-      };
-      auto issue_pv = [&](int m, int s, int kchunks, bool accumulate) {
-        const uint32_t d = tbase + m * 256 + 128;
-        const uint32_t a = tbase + m * 256;
-        const uint64_t b0 = s ? dV1 : dV0;
-#pragma unroll
-        for (int k = 0; k < kTcBN / 16; ++k) {
-          if (k < kchunks) mma_ts(d, a + k * 8, b0 + k * (2048 / 16), idO, (accumulate || k > 0) ? 1u : 0u);
-        }
-      };
+      // descriptors built once; each K step only adds a compile-time offset
+      // (the start-address field is the low 14 bits, in 16-byte units, and
+      // shared-memory addresses stay below 256 KB, so it never carries out)
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ) + m * C::kHalves * C::kQHalfBytes, 16, 1024);
+      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::kKvHalfBytes, 1024);
+      const uint32_t tO = tbase + m * 128;
+      uint32_t hc = 0, hb = 0, qs = 0, pcnt[2] = {0, 0}, of = 0;
+      bool used = false, ok = true;
       for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
            g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
         if (g.skip) continue;
         if (!(ok = mbar_wait(&bars.q_full, qs & 1, abort))) break;
         ++qs;
-        tc_fence_after();
-        const int nt = g.tile1 - g.tile0;
-        const long long end = static_cast<long long>(g.plen) + g.n;
-        bool pv_started[2] = {false, false};
-        // Ping-pong order per step i: PV_0(i-1), S_0(i), PV_1(i-1), S_1(i).
-        // S_m(i) reuses the Tensor Memory columns P_m(i-1) occupies, so it is
-        // issued after PV_m(i-1); tcgen05 MMAs from one thread run in order.
-        // A PV never waits for the next K tile.
-        for (int i = 0; i <= nt && ok; ++i) {
-          const uint32_t iti = it + i;
-          const int s = iti % kTcStages;
-          const int sp = (iti - 1) % kTcStages;
-          int kch = 0;
-          if (i > 0) {
-            const long long hi = min(end, static_cast<long long>(g.tile0 + i) * kTcBN);
-            kch = static_cast<int>((hi - static_cast<long long>(g.tile0 + i - 1) * kTcBN + 15) / 16);
+        const int nh = tc_steps(g);
+        if (m >= g.mt) {
+          // no rows here: pace the hand-off on the stages' fills, then release them
+          for (int j = 0; j < nh && ok; ++j) {
+            const uint32_t h = hc + j;
+            if (!(ok = mbar_wait(&bars.kv_full[h % kTcStages], (h / kTcStages) & 1, abort))) break;
+            mbar_arrive(&bars.kv_empty[h % kTcStages]);
+            if (j == nh - 1) mbar_arrive(&bars.q_empty);
           }
-          for (int m = 0; m < g.mt && ok; ++m) {
-            if (i > 0) {
-              if (!(ok = mbar_wait(&bars.p_ready[m], pc[m] & 1, abort))) break;
-              ++pc[m];
-              if (!pv_started[m] && used[m]) {
-                if (!(ok = mbar_wait(&bars.o_free[m], of[m] & 1, abort))) break;
-                ++of[m];
-              }
-              if (m == 0 && !(ok = mbar_wait(&bars.v_full[sp], ((iti - 1) / kTcStages) & 1, abort))) break;
-              tc_fence_after();
-              issue_pv(m, sp, kch, pv_started[m]);
-              pv_started[m] = true;
-              if (i == nt) mma_commit(&bars.o_done[m]);
-            }
-            if (i < nt) {
-              if (m == 0) {
-                if (!(ok = mbar_wait(&bars.k_full[s], (iti / kTcStages) & 1, abort))) break;
-                tc_fence_after();
-              }
-              issue_s(m, s);
-            }
-          }
-          if (!ok) break;
-          if (i > 0) mma_commit(&bars.v_empty[sp]);
-          if (i < nt) mma_commit(&bars.k_empty[s]);
-          if (i == nt - 1) mma_commit(&bars.q_empty);    // the last S of the segment
+          hc += nh;
+          continue;
         }
-        for (int m = 0; m < g.mt; ++m) used[m] = true;
-        it += nt;
+        tc_fence_after();
+        const long long end = static_cast<long long>(g.plen) + g.n;
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t h = hc + j;
+          const int s = h % kTcStages;
+          if (!mbar_wait(&bars.kv_full[s], (h / kTcStages) & 1, abort)) return false;
+          tc_fence_after();
+          const int b = (hb + j) & 1;
+          const uint32_t tS = tbase + 256 + m * 128 + b * 64;
+          const uint64_t bk = dK + s * (C::kStageBytes / 16);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)                      // 32 bytes per K step
+            mma_ss(tS, dQ + (k / 4) * (C::kQHalfBytes / 16) + (k % 4) * 2,
+                   bk + (k / 4) * (C::kKvHalfBytes / 16) + (k % 4) * 2, idS, k > 0 ? 1u : 0u);
+          mma_commit(&bars.s_ready[m][b]);
+          if (j == nh - 1) mma_commit(&bars.q_empty);           // the last S of the segment
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && nh > 1) ok = issue_s(1);
+        for (int j = 0; j < nh && ok; ++j) {
+          const uint32_t h = hc + j;
+          const int s = h % kTcStages;
+          const int b = (hb + j) & 1;
+          if (!(ok = mbar_wait(&bars.p_ready[m][b], pcnt[b] & 1, abort))) break;
+          ++pcnt[b];
+          if (j == 0 && used) {
+            if (!(ok = mbar_wait(&bars.o_free[m], of & 1, abort))) break;
+            ++of;
+          }
+          tc_fence_after();                                     // K + V of the step landed before S(j)
+          const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
+          const int kch = static_cast<int>((min(end, k0 + kTcBK) - k0 + 15) / 16);
+          const uint32_t tP = tbase + 256 + m * 128 + b * 64;
+          const uint64_t bv = dV + s * (C::kStageBytes / 16);
+#pragma unroll
+          for (int k = 0; k < kTcBK / 16; ++k)                  // 16 keys (2048 B of V) per step
+            if (k < kch) mma_ts(tO, tP + k * 8, bv + k * (2048 / 16), idO, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars.kv_empty[s]);
+          if (j == nh - 1) mma_commit(&bars.o_done[m]);
+          if (j + 2 < nh) ok = issue_s(j + 2);
+        }
+        used = true;
+        hc += nh;
+        hb += nh;
       }
-      // drain: every MMA issued so far completes before Tensor Memory is freed
-      mma_commit(&bars.drain);
+      // drain: every MMA this thread issued completes before Tensor Memory is freed
+      mma_commit(&bars.drain[m]);
       volatile int no_abort = 0;
-      mbar_wait(&bars.drain, 0, &no_abort);
+      mbar_wait(&bars.drain[m], 0, &no_abort);
     }
-  } else {
+  } else if (warp >= 4) {
     // ================================================= softmax groups
-    const int m = (warp - 3) >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + m * 256 + lane_addr;
-    const uint32_t tO = tS + 128;
-    uint32_t sc = 0, oc = 0;
+    // warps 4-7 serve M tile 0, warps 8-11 M tile 1; warp w owns Tensor
+    // Memory lanes 32 * (w % 4) .. +31, one query row per thread.
+    const int m = (warp - 4) >> 2;
+    const int qd = warp & 3;
+    const int j4 = 4 * m + qd;                         // quarter of the unit's rows
+    const uint32_t lane_addr = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t tO = tbase + m * 128 + lane_addr;
+    uint32_t hb = 0, hcs = 0, scnt[2] = {0, 0}, oc = 0;
     bool ok = true;
     for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
          g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
       if (g.skip) continue;
-      const int nt = g.tile1 - g.tile0;
-      const int nd = g.node0 + m * npm + row / G;    // node of this row
-      const bool row_valid = m < g.mt && row < G * npm && nd < g.n;
-      const bool warp_live = __any_sync(0xffffffffu, row_valid);
-      float m_ref = -INFINITY, l_sum = 0.f;
-      if (m < g.mt) {
-        const uint32_t* mrow = p.mask + static_cast<size_t>(g.t0 + (row_valid ? nd : 0)) * p.words;
-        for (int i = 0; i < nt && ok; ++i) {
-          if (!(ok = mbar_wait(&bars.s_ready[m], sc & 1, abort))) break;
-          ++sc;
-          tc_fence_after();
-          if (warp_live) {
-            const int k0 = (g.tile0 + i) * kTcBN;
-            float s[kTcBN];
-            uint32_t* su = reinterpret_cast<uint32_t*>(s);
+      const int nh = tc_steps(g);
+      if (m >= g.mt) {
+        hcs += nh;
+        continue;
+      }
+      const RowSplit rs = row_split(g.nodes, g.mt);
+      const int cnt = quarter_count(rs, j4);
+      const bool warp_live = cnt > 0;                  // uniform over the warp
+      const bool row_valid = lane < G * cnt;
+      const int nd = g.node0 + quarter_first(rs, j4) + (row_valid ? lane / G : 0);   // node of this row
+      float m_ref = -INFINITY, l_a = 0.f, l_b = 0.f;
+      const uint32_t* mrow = p.mask + static_cast<size_t>(g.t0 + nd) * p.words;
+      for (int j = 0; j < nh && ok; ++j) {
+        const int b = (hb + j) & 1;
+        if (!(ok = mbar_wait(&bars.s_ready[m][b], scnt[b] & 1, abort))) break;
+        ++scnt[b];
+        tc_fence_after();
+        if (warp_live) {
+          const uint32_t tS = tbase + 256 + m * 128 + b * 64 + lane_addr;
+          const int k0 = g.tile0 * kTcBN + j * kTcBK;
+          uint32_t a[kTcBK];
+          tmem_ld32(tS, a);
+          tmem_ld32(tS + 32, a + 32);
+          tmem_ld_wait();
+          if (k0 + kTcBK > g.plen) {                   // the step reaches past the prompt: mask it
 #pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
-            tmem_ld_wait();
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) {
+            for (int c = 0; c < kTcBK / 32; ++c) {
               const uint32_t vis = row_valid ? visible_bits(mrow, p.words, g.plen, g.n, k0 + c * 32) : 0u;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float v = ((vis >> e) & 1u) ? s[c * 32 + e] : -INFINITY;
-                s[c * 32 + e] = v;
-                mx = fmaxf(mx, v);
-              }
+              for (int e = 0; e < 32; ++e)
+                if (!((vis >> e) & 1u)) a[c * 32 + e] = 0xFF800000u;   // -inf
             }
-            // Lazy rescale: keep the reference max until a score exceeds it by
-            // 2^8; p stays <= 2^8 and O, l share the same reference.
-            const float mxs = mx * p.scale_log2;
-            float alpha = 1.f;
-            if (mxs > m_ref + 8.f) {
-              alpha = (i > 0 && m_ref != -INFINITY) ? fast_exp2(m_ref - mxs) : 1.f;
-              l_sum *= alpha;
-              m_ref = mxs;
-            }
-            const float base = m_ref == -INFINITY ? 0.f : m_ref;
+          }
+          float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * e], p.scale_log2, -base));
-                const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * e + 1], p.scale_log2, -base));
-                l_sum += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
-              }
-              tmem_st16(tS + c * 16, pk);
-            }
-            if (alpha != 1.f) {                         // O holds earlier tiles: rescale it
+          for (int e = 0; e < kTcBK; e += 8) {
+            x0 = fmax3(x0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+            x1 = fmax3(x1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+            x2 = fmax3(x2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+            x3 = fmax3(x3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+          }
+          const float mxs = fmax3(x0, x1, fmaxf(x2, x3)) * p.scale_log2;
+          // Lazy rescale: keep the reference max until a score exceeds it by
+          // 2^8; p stays <= 2^8 and O, l share the same reference. O is only
+          // rescaled once PV(j - 1), the last MMA that adds to it, is done.
+          if (mxs > m_ref + 8.f) {
+            if (m_ref != -INFINITY) {
+              const float alpha = fast_exp2(m_ref - mxs);
+              l_a *= alpha;
+              l_b *= alpha;
+              const uint32_t hp = hcs + j - 1;                  // the step whose PVs last added to O
+              ok = mbar_wait(&bars.kv_empty[hp % kTcStages], (hp / kTcStages) & 1, abort);
+              tc_fence_after();
 #pragma unroll 1
               for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -671,65 +744,93 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                 tmem_st32(tO + c * 32, o);
               }
             }
-            tmem_st_wait();
+            m_ref = mxs;
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.p_ready[m]);
+          const float base = m_ref == -INFINITY ? 0.f : m_ref;
+          // p = 2^(s * scale * log2(e) - base) as bf16 into the buffer's first 32 columns
+#pragma unroll
+          for (int c = 0; c < kTcBK / 32; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float y0 = fmaf(__uint_as_float(a[c * 32 + 2 * e]), p.scale_log2, -base);
+              const float y1 = fmaf(__uint_as_float(a[c * 32 + 2 * e + 1]), p.scale_log2, -base);
+              // one pair in kExpFmaEvery on the FMA pipe, the rest on MUFU
+              const bool on_fma = kExpFmaEvery > 0 && e % kExpFmaEvery == kExpFmaEvery - 1;
+              const float p0 = on_fma ? exp2_fma(y0) : fast_exp2(y0);
+              const float p1 = on_fma ? exp2_fma(y1) : fast_exp2(y1);
+              l_a += p0;
+              l_b += p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
+          }
+          tmem_st_wait();
         }
-        if (ok && (ok = mbar_wait(&bars.o_done[m], oc & 1, abort))) {
-          ++oc;
-          tc_fence_after();
-          if (warp_live) {
-            const int h = g.kvh * G + row % G;
-            if (g.whole) {
-              __nv_bfloat16* dst = p.out + (static_cast<size_t>(g.t0 + nd) * p.hq + h) * D;
-              const float inv = 1.f / l_sum;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_ready[m][b]);
+      }
+      hb += nh;
+      hcs += nh;
+      if (ok && (ok = mbar_wait(&bars.o_done[m], oc & 1, abort))) {
+        ++oc;
+        tc_fence_after();
+        if (warp_live) {
+          const float l_sum = l_a + l_b;
+          const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+          if (g.whole) {
+            const int h = g.kvh * G + lane % G;
+            __nv_bfloat16* dst = p.out + (static_cast<size_t>(g.t0 + nd) * p.hq + h) * D;
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait();
-                if (row_valid) {
-                  uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    d4[q] = make_uint4(
-                        pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                        pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                        pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                        pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-                }
-              }
-            } else {
-              // partial of a split unit, stored column-block major so the
-              // 128 rows of a group write (and the merge reads) contiguously
-              float4* part = reinterpret_cast<float4*>(p.partials + static_cast<size_t>(g.my_slot) * kSlotFloats(D));
-              const int r = m * 128 + row;
-#pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait();
-                if (row_valid) {
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-                    part[(c * 8 + q) * 256 + r] =
-                        make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                    __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
-                }
-              }
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
               if (row_valid) {
-                float* ml = reinterpret_cast<float*>(part + (D / 4) * 256);
-                ml[r] = m_ref;
-                ml[256 + r] = l_sum;
+                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  d4[q] = make_uint4(
+                      pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                      pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                      pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                      pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
               }
             }
+          } else {
+            // partial of a split unit: O / l as fp16 (a convex combination of
+            // value rows, so well inside fp16 range) in [D/8 column blocks]
+            // [256 rows] 16-byte vectors, so a quarter's 32 rows write (and the
+            // merge reads) 512 contiguous bytes; then the row's m and l
+            uint8_t* slot = p.partials + static_cast<size_t>(g.my_slot) * kSlotBytes(D);
+            uint4* o16 = reinterpret_cast<uint4*>(slot);
+            const int r = j4 * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+              if (row_valid) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  o16[(c * 4 + q) * 256 + r] = make_uint4(
+                      pack_half2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                      pack_half2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                      pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                      pack_half2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+              }
+            }
+            if (row_valid) {
+              float* ml = reinterpret_cast<float*>(slot + static_cast<size_t>(256) * 2 * D);
+              ml[r] = m_ref;
+              ml[256 + r] = l_sum;
+            }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.o_free[m]);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.o_free[m]);
       }
       if (!ok) break;
     }
@@ -762,6 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       rec[7] = blockIdx.x;                                              // first contributor
       rec[8] = tc_cta_of(total, p.grid, last.unit_t0 + last.ntiles - 1); // last contributor
       rec[9] = last.my_slot;                                            // its slot
+      rec[10] = last.nodes;
     }
     rec[0] = valid;
   }
@@ -770,49 +872,55 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 // ------------------------------------------------------------ merge of split units
 //
 // A unit whose key tiles were cut between CTAs c_first..c_last left one
-// partial (unnormalised O, reference max m, sum l, all per row) per
-// contributor. Merging is the usual log-sum-exp combination:
-//   out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,  M = max_c m_c.
-// kMergeSplit CTAs per split unit (32 rows each, 8 threads per row); each
-// thread loads kMergeChunk contributors' partials at once.
+// partial (normalised o_c = O_c / l_c, reference max m_c, sum l_c, per row)
+// per contributor. The merge is the usual log-sum-exp combination:
+//   out = sum_c w_c o_c / sum_c w_c,  w_c = 2^(m_c - M) l_c,  M = max_c m_c.
+// kMergeSplit CTAs per split unit, one per quarter of its rows (32 rows, 8
+// threads per row); each thread loads kMergeChunk contributors at once.
 
 struct MergeParams {
   const int32_t* tasks;
-  const float* partials;
+  const uint8_t* partials;
   __nv_bfloat16* out;
-  int hq, group, npm;
+  int hq, group;
 };
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeSplit = 8;      // CTAs per unit (32 rows each)
+constexpr int kMergeSplit = 8;      // CTAs per unit: one per row quarter
 constexpr int kMergeChunk = 4;      // contributors whose loads are in flight together
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   grid_dependency_wait();            // the attention grid's partials and tasks are visible
-  const int c = blockIdx.x / kMergeSplit, part_cta = blockIdx.x % kMergeSplit;
+  const int c = blockIdx.x / kMergeSplit, j = blockIdx.x % kMergeSplit;
   const int32_t* rec = p.tasks + c * kTaskInts;
   if (rec[0] == 0) return;
-  const int kvh = rec[2], node0 = rec[3], mt = rec[4], t0 = rec[5], n = rec[6];
-  const int c_first = rec[7], c_last = rec[8], first_slot = rec[9];
-  constexpr int kRowsCta = 256 / kMergeSplit;         // 32 rows per CTA
-  constexpr int kParts = kMergeThreads / kRowsCta;    // 8 threads per row
-  constexpr int kVecs = D / 4 / kParts;               // float4 per thread
-  const int r = part_cta * kRowsCta + threadIdx.x % kRowsCta;
-  const int part = threadIdx.x / kRowsCta;
-  const int mm = r >> 7, rr = r & 127;
+  const int kvh = rec[2], node0 = rec[3], mt = rec[4], t0 = rec[5];
+  const int c_first = rec[7], c_last = rec[8], first_slot = rec[9], nodes = rec[10];
+  if ((j >> 2) >= mt) return;
   const int G = p.group;
-  const int nd = node0 + mm * p.npm + rr / G;
-  if (mm >= mt || rr >= G * p.npm || nd >= n) return;
+  const RowSplit rs = row_split(nodes, mt);
+  const int cnt = quarter_count(rs, j);
+  constexpr int kParts = kMergeThreads / 32;          // 8 threads per row
+  constexpr int kVecs = D / 8 / kParts;               // 16-byte vectors (8 fp16) per thread
+  const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
+  if (lane >= G * cnt) return;
+  const int nd = node0 + quarter_first(rs, j) + lane / G;
+  const int r = j * 32 + lane;
   const int nc = c_last - c_first + 1;
-  // single pass, online log-sum-exp over chunks of contributors
   float m_run = -INFINITY, l_run = 0.f;
-  float4 acc[kVecs];
+  float acc[kVecs][8];
 #pragma unroll
-  for (int v = 0; v < kVecs; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int v = 0; v < kVecs; ++v)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[v][e] = 0.f;
   for (int k0 = 0; k0 < nc; k0 += kMergeChunk) {
     float mc[kMergeChunk], lc[kMergeChunk];
-    float4 x[kMergeChunk][kVecs];
+    uint4 x[kMergeChunk][kVecs];
 #pragma unroll
     for (int u = 0; u < kMergeChunk; ++u) {
       const int k = k0 + u;
@@ -820,12 +928,13 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_
       lc[u] = 0.f;
       if (k < nc) {
         const int sl = k == 0 ? first_slot : 2 * (c_first + k);
-        const float* base = p.partials + static_cast<size_t>(sl) * kSlotFloats(D);
-        mc[u] = __ldcg(base + D * 256 + r);
-        lc[u] = __ldcg(base + D * 256 + 256 + r);
-        const float4* o4 = reinterpret_cast<const float4*>(base);
+        const uint8_t* base = p.partials + static_cast<size_t>(sl) * kSlotBytes(D);
+        const float* ml = reinterpret_cast<const float*>(base + static_cast<size_t>(256) * 2 * D);
+        mc[u] = __ldcg(ml + r);
+        lc[u] = __ldcg(ml + 256 + r);
+        const uint4* o16 = reinterpret_cast<const uint4*>(base);
 #pragma unroll
-        for (int v = 0; v < kVecs; ++v) x[u][v] = __ldcg(o4 + (part * kVecs + v) * 256 + r);
+        for (int v = 0; v < kVecs; ++v) x[u][v] = __ldcg(o16 + (part * kVecs + v) * 256 + r);
       }
     }
     float m_new = m_run;
@@ -835,35 +944,34 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_
     const float sc = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
     l_run *= sc;
 #pragma unroll
-    for (int v = 0; v < kVecs; ++v) {
-      acc[v].x *= sc;
-      acc[v].y *= sc;
-      acc[v].z *= sc;
-      acc[v].w *= sc;
-    }
+    for (int v = 0; v < kVecs; ++v)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[v][e] *= sc;
 #pragma unroll
     for (int u = 0; u < kMergeChunk; ++u) {
       if (mc[u] == -INFINITY) continue;
-      const float w = fast_exp2(mc[u] - m_new);
-      l_run += w * lc[u];
+      const float w = fast_exp2(mc[u] - m_new) * lc[u];
+      l_run += w;
 #pragma unroll
       for (int v = 0; v < kVecs; ++v) {
-        acc[v].x += w * x[u][v].x;
-        acc[v].y += w * x[u][v].y;
-        acc[v].z += w * x[u][v].z;
-        acc[v].w += w * x[u][v].w;
+        const uint32_t xs[4] = {x[u][v].x, x[u][v].y, x[u][v].z, x[u][v].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = half2_to_float2(xs[e]);
+          acc[v][2 * e] = fmaf(w, f.x, acc[v][2 * e]);
+          acc[v][2 * e + 1] = fmaf(w, f.y, acc[v][2 * e + 1]);
+        }
       }
     }
     m_run = m_new;
   }
-  const float inv = 1.f / l_run;
-  const int h = kvh * G + rr % G;
-  uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(t0 + nd) * p.hq + h) * D +
-                                        part * kVecs * 4);
+  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+  const int h = kvh * G + lane % G;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(t0 + nd) * p.hq + h) * D) + part * kVecs;
 #pragma unroll
   for (int v = 0; v < kVecs; ++v)
-    dst[v] = make_uint2(pack_bf16x2(acc[v].x * inv, acc[v].y * inv),
-                        pack_bf16x2(acc[v].z * inv, acc[v].w * inv));
+    dst[v] = make_uint4(pack_bf16x2(acc[v][0] * inv, acc[v][1] * inv), pack_bf16x2(acc[v][2] * inv, acc[v][3] * inv),
+                        pack_bf16x2(acc[v][4] * inv, acc[v][5] * inv), pack_bf16x2(acc[v][6] * inv, acc[v][7] * inv));
 }
 
 // ------------------------------------------------------------ host
@@ -894,15 +1002,15 @@ static bool encode_4d(CUtensorMap* map, void* base, const cuuint64_t dims[4],
 
 struct TcLayout {
   size_t task_bytes, partial_bytes, qrot_bytes, total;
-  int npm;
+  int npq;
 };
 
 static TcLayout tc_layout(int batch, int hq, int hkv, int max_nodes, int head_dim, int grid) {
   TcLayout L;
   const int group = hq / hkv;
-  L.npm = 128 / group;
+  L.npq = 32 / group;
   L.task_bytes = (static_cast<size_t>(grid) * kTaskInts * sizeof(int32_t) + 255) / 256 * 256;
-  L.partial_bytes = static_cast<size_t>(2) * grid * kSlotFloats(head_dim) * sizeof(float);
+  L.partial_bytes = static_cast<size_t>(2) * grid * kSlotBytes(head_dim);
   L.partial_bytes = (L.partial_bytes + 255) / 256 * 256;
   L.qrot_bytes = static_cast<size_t>(batch) * max_nodes * hq * head_dim * 2;
   L.total = L.task_bytes + L.partial_bytes + L.qrot_bytes;
@@ -966,7 +1074,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(group) * D * 2,
                                    static_cast<cuuint64_t>(hq) * D * 2};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(group), 1, static_cast<cuuint32_t>(L.npm)};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(group), 1, static_cast<cuuint32_t>(L.npq)};
     if (!encode_4d(&tp.qmap, q_rot, dims, strides, box)) return TV_ERR_CUDA;
   }
   {
@@ -986,7 +1094,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   tp.status = status;
   tp.out = static_cast<__nv_bfloat16*>(out);
   tp.tasks = reinterpret_cast<int32_t*>(ws);
-  tp.partials = reinterpret_cast<float*>(ws + L.task_bytes);
+  tp.partials = reinterpret_cast<uint8_t*>(ws + L.task_bytes);
   tp.status_rw = status;
   tp.batch = batch;
   tp.max_nodes = max_nodes;
@@ -994,7 +1102,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   tp.hq = hq;
   tp.hkv = hkv;
   tp.group = group;
-  tp.npm = L.npm;
+  tp.npq = L.npq;
   tp.words = (max_nodes + 31) / 32;
   tp.max_blocks = max_blocks;
   tp.grid = grid;
@@ -1007,7 +1115,6 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   mp.out = tp.out;
   mp.hq = hq;
   mp.group = group;
-  mp.npm = L.npm;
 
   const dim3 rgrid((max_nodes + kRopeNodes - 1) / kRopeNodes, batch);
   static size_t smem_set128[kMaxDevices] = {0}, smem_set64[kMaxDevices] = {0};
