@@ -52,7 +52,7 @@ constexpr int kTcStages = 4;        // K/V pipeline depth, in steps
 constexpr int kTcThreads = 384;     // 12 warps
 constexpr int kExpFmaEvery = 0;     // one exponential pair in this many on the FMA pipe (0: none)
 constexpr int kTcMaxBatch = 4096;
-constexpr int kRopeNodes = 4;       // nodes per pre-pass CTA
+constexpr int kRopeNodes = 1;       // nodes per pre-pass CTA
 constexpr int kRopeBatch = 4;       // loads in flight per pre-pass thread
 constexpr int kRopeThreads = 256;
 constexpr int kTaskInts = 16;       // merge-task record per attention CTA
@@ -102,41 +102,49 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
   constexpr int D2 = D / 2;
   __shared__ float2 s_cs[kRopeNodes][D2];
   __shared__ int s_blk[kRopeNodes];      // cache block of each node's tentative slot
+  grid_dependency_wait();                // inputs written by the previous kernel are visible
   grid_launch_dependents();              // the attention grid may start its prologue
   const int b = blockIdx.y;
+  // the request's scalars, loaded together (one memory round trip)
   const int t0 = p.cu_nodes[b];
-  const int n = p.cu_nodes[b + 1] - t0;
+  const int t1 = p.cu_nodes[b + 1];
   const int plen = p.prompt_len[b];
+  const int st = p.status[b];
+  const int held = p.n_blocks[b];
+  const int n = t1 - t0;
   if (n < 1 || n > p.max_nodes || plen < 0) return;             // tree_build flagged it
   if (static_cast<long long>(t0) + n > p.t_cap || t0 < 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_SIZE);
     return;
   }
-  if (p.status[b] & TV_TREE_FLAGS) return;
+  if (st & TV_TREE_FLAGS) return;
   const int i0 = blockIdx.x * kRopeNodes;
   if (i0 >= n) return;
   const int i1 = min(n, i0 + kRopeNodes);
-  // every block holding slots [0, P + n) must be held and in range
+  // every block holding slots [0, P + n) must be held and in range (the
+  // loads of a thread are independent, so they are all in flight at once)
   const long long slots = static_cast<long long>(plen) + n;
   const int nlb = static_cast<int>((slots + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
   const int32_t* trow = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-  int bad = (nlb > p.n_blocks[b] || nlb > p.max_blocks) ? 1 : 0;
-  for (int lb = threadIdx.x; !bad && lb < nlb; lb += blockDim.x) {
-    const int blk = trow[lb];
-    if (blk < 0 || blk >= p.num_blocks) bad = 1;
+  int bad = (nlb > held || nlb > p.max_blocks) ? 1 : 0;
+  if (!bad) {
+#pragma unroll 8
+    for (int lb = threadIdx.x; lb < nlb; lb += blockDim.x) {
+      const int blk = trow[lb];
+      bad |= (blk < 0 || blk >= p.num_blocks) ? 1 : 0;
+    }
   }
-  if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
-    return;
-  }
-  if (threadIdx.x < i1 - i0) s_blk[threadIdx.x] = trow[(plen + i0 + threadIdx.x) / TV_BLOCK_SIZE];
+  if (threadIdx.x < i1 - i0) s_blk[threadIdx.x] = bad ? 0 : trow[(plen + i0 + threadIdx.x) / TV_BLOCK_SIZE];
   for (int idx = threadIdx.x; idx < (i1 - i0) * D2; idx += blockDim.x) {
     const int nd = idx / D2, pr = idx % D2;
     float sn, cs;
     sincosf(static_cast<float>(p.positions[t0 + i0 + nd]) * p.inv_freq[pr], &sn, &cs);
     s_cs[nd][pr] = make_float2(cs, sn);
   }
-  __syncthreads();
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
+    return;
+  }
   const bool style0 = p.rope_style == 0;
   // Work item = one 16-byte vector (8 bf16) of one head of one node; style 0
   // rotates the pairs inside the vector, style 1 pairs vector v with vector
@@ -896,6 +904,7 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t v) {
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   grid_dependency_wait();            // the attention grid's partials and tasks are visible
+  grid_launch_dependents();
   const int c = blockIdx.x / kMergeSplit, j = blockIdx.x % kMergeSplit;
   const int32_t* rec = p.tasks + c * kTaskInts;
   if (rec[0] == 0) return;
@@ -1144,14 +1153,14 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   mcfg.dynamicSmemBytes = 0;
   cudaError_t err;
   if (D == 128) {
-    rope_append_kernel<128><<<rgrid, kRopeThreads, 0, stream>>>(rp);
     if (!ensure_smem(attn_tc_kernel<128>, smem, smem_set128, dev)) return TV_ERR_CUDA;
-    err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<128>, tp);
+    err = launch_pdl(rope_append_kernel<128>, rgrid, dim3(kRopeThreads), 0, stream, rp);
+    if (err == cudaSuccess) err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<128>, tp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&mcfg, attn_merge_kernel<128>, mp);
   } else {
-    rope_append_kernel<64><<<rgrid, kRopeThreads, 0, stream>>>(rp);
     if (!ensure_smem(attn_tc_kernel<64>, smem, smem_set64, dev)) return TV_ERR_CUDA;
-    err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<64>, tp);
+    err = launch_pdl(rope_append_kernel<64>, rgrid, dim3(kRopeThreads), 0, stream, rp);
+    if (err == cudaSuccess) err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<64>, tp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&mcfg, attn_merge_kernel<64>, mp);
   }
   if (err != cudaSuccess) return TV_ERR_CUDA;

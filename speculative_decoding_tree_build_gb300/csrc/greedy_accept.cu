@@ -31,10 +31,13 @@ greedy_accept_kernel(const int32_t* __restrict__ target_ids,
   __shared__ int s_next[TV_MAX_NODES];
   __shared__ int s_path[TV_MAX_NODES];
   __shared__ int s_len, s_bonus, s_bad;
+  grid_dependency_wait();                 // inputs written by the previous kernel are visible
+  grid_launch_dependents();
   const int b = blockIdx.x;
-  if (status[b] != 0) return;
+  const int st = status[b];               // loaded together with the node range
   const int t0 = cu_nodes[b];
   const int n = cu_nodes[b + 1] - t0;
+  if (st != 0) return;
   if (n < 1 || n > max_nodes) {
     if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
     return;
@@ -97,8 +100,9 @@ extern "C" int tv_greedy_accept(const int32_t* target_ids, const int32_t* draft_
   if (!target_ids || !draft_tokens || !cu_nodes || !next_token || !next_sibling ||
       !accept_path || !accept_len || !bonus || !status)
     return TV_ERR_NULL_POINTER;
-  tv::greedy_accept_kernel<<<batch, tv::kAcceptThreads, 0, tv::as_stream(stream)>>>(
-      target_ids, draft_tokens, cu_nodes, next_token, next_sibling, max_nodes, max_depth,
-      accept_path, accept_len, bonus, status);
-  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+  const cudaError_t err = tv::launch_pdl(tv::greedy_accept_kernel, dim3(batch), dim3(tv::kAcceptThreads), 0,
+                                         tv::as_stream(stream), target_ids, draft_tokens, cu_nodes,
+                                         next_token, next_sibling, static_cast<int>(max_nodes),
+                                         static_cast<int>(max_depth), accept_path, accept_len, bonus, status);
+  return err == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }

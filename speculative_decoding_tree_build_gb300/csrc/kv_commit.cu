@@ -33,22 +33,25 @@ kv_commit_kernel(const int32_t* __restrict__ accept_path, const int32_t* __restr
   __shared__ int s_path[TV_MAX_NODES];
   __shared__ int s_blk[2 * TV_MAX_NODES];
   __shared__ int s_bad;
+  grid_dependency_wait();                 // inputs written by the previous kernel are visible
+  grid_launch_dependents();
   const int b = blockIdx.x;
-  if (status[b] != 0) return;
+  // one memory round trip: the request's scalars and its whole path row
+  // (max_depth + 1 entries, valid memory whatever the accepted length)
+  const int st = status[b];
   const int a = accept_len[b];
   const int plen = prompt_len[b];
-  const int held0 = n_blocks[b];
-  if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0 || held0 < 0 || held0 > max_blocks) {
+  const int held = n_blocks[b];
+  const int32_t* path = accept_path + static_cast<size_t>(b) * (max_depth + 1);
+  for (int k = threadIdx.x; k <= max_depth && k < TV_MAX_NODES; k += blockDim.x) s_path[k] = path[k];
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (st != 0) return;
+  if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0 || held < 0 || held > max_blocks) {
     if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
     return;
   }
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  const int32_t* path = accept_path + static_cast<size_t>(b) * (max_depth + 1);
   const int32_t* table = block_table + static_cast<size_t>(b) * max_blocks;
-  const int held = n_blocks[b];
-  for (int k = threadIdx.x; k <= a; k += blockDim.x) s_path[k] = path[k];
-  __syncthreads();
   int bad = 0;
   for (int k = threadIdx.x; k <= a; k += blockDim.x) {
     const int pk = s_path[k];
@@ -147,9 +150,10 @@ extern "C" int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* a
   if (dev < 0) return TV_ERR_CUDA;
   if (!tv::ensure_smem(tv::kv_commit_kernel, tv::kCommitSmem, smem_set, dev)) return TV_ERR_CUDA;
   const int head_vecs = geom->head_dim / 8;
-  tv::kv_commit_kernel<<<batch, tv::kCommitThreads, tv::kCommitSmem, tv::as_stream(stream)>>>(
-      accept_path, accept_len, max_depth, prompt_len, block_table, n_blocks, max_blocks_per_req,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks,
-      geom->num_kv_heads, head_vecs, new_len, released, released_count, status);
-  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+  const cudaError_t err = tv::launch_pdl(
+      tv::kv_commit_kernel, dim3(batch), dim3(tv::kCommitThreads), tv::kCommitSmem, tv::as_stream(stream),
+      accept_path, accept_len, static_cast<int>(max_depth), prompt_len, block_table, n_blocks,
+      static_cast<int>(max_blocks_per_req), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      static_cast<int>(num_blocks), geom->num_kv_heads, head_vecs, new_len, released, released_count, status);
+  return err == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }

@@ -25,6 +25,8 @@ tree_build_kernel(const int32_t* __restrict__ parents, const int32_t* __restrict
   __shared__ int s_par[TV_MAX_NODES];
   __shared__ int s_child[TV_MAX_NODES];
   __shared__ int s_bad;
+  grid_dependency_wait();                 // inputs written by the previous kernel are visible
+  grid_launch_dependents();
   const int b = blockIdx.x;
   const int t0 = cu_nodes[b];
   const int n = cu_nodes[b + 1] - t0;
@@ -111,8 +113,9 @@ extern "C" int tv_tree_build(const int32_t* parents, const int32_t* cu_nodes,
       !retrieve_index || !next_token || !next_sibling || !status)
     return TV_ERR_NULL_POINTER;
   const int words = (max_nodes + 31) / 32;
-  tv::tree_build_kernel<<<batch, tv::kBuildThreads, 0, tv::as_stream(stream)>>>(
-      parents, cu_nodes, prompt_len, max_nodes, words, mask_bits, depth, positions,
-      retrieve_index, next_token, next_sibling, status);
-  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+  const cudaError_t err = tv::launch_pdl(tv::tree_build_kernel, dim3(batch), dim3(tv::kBuildThreads), 0,
+                                         tv::as_stream(stream), parents, cu_nodes, prompt_len,
+                                         static_cast<int>(max_nodes), words, mask_bits, depth, positions,
+                                         retrieve_index, next_token, next_sibling, status);
+  return err == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }

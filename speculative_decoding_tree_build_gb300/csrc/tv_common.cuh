@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/treeverify.h"
 
 #define TV_TREE_FLAGS (TV_ST_BAD_SIZE | TV_ST_BAD_ROOT | TV_ST_BAD_PARENT)
@@ -96,6 +98,41 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start while the previous grid on the stream runs; it
+// must wait here before touching anything that grid reads or writes.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid on the stream (if launched programmatically) to start
+// being scheduled; its CTAs still wait in grid_dependency_wait.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- host launch
+
+// Launch with programmatic stream serialisation. Every kernel launched this
+// way calls grid_dependency_wait() before its first global memory access, so
+// stream order is kept; what is gained is the launch latency, which overlaps
+// the previous grid's tail.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace tv

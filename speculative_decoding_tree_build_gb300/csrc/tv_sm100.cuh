@@ -69,11 +69,10 @@ __device__ __forceinline__ bool mbar_poll64(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Returns false (and
-// raises *abort) when the wait runs past kWaitLimitCycles or another role
-// has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_poll64(bar, parity)) return true;
+// Slow path of mbar_wait, kept out of line so every wait site stays a few
+// instructions long (the warps of one CTA run different code; small loops
+// keep the instruction cache warm).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
     if (mbar_poll64(bar, parity)) return true;
@@ -89,6 +88,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Wait for the phase with the given parity to complete. Returns false (and
+// raises *abort) when the wait runs past kWaitLimitCycles or another role
+// has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 // ----------------------------------------------------------------------- TMA
@@ -223,19 +230,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
-}
-
-// Programmatic dependent launch: a grid launched with programmatic stream
-// serialisation may start while the previous grid on the stream runs; it
-// must wait here before touching anything that grid writes.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Allow the next grid on the stream (if launched programmatically) to start
-// its prologue.
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace tv
