@@ -95,3 +95,31 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 41, *mis) == -5
     assert L.tv_workspace_bytes(ctypes.byref(bad_d), 1, 41, ctypes.byref(ctypes.c_size_t())) == -2
     assert L.tv_workspace_bytes(ctypes.byref(g), 1, 41, None) == -1
+
+
+def test_fma_exp2_cubic_error_bound():
+    """The cubic that can replace MUFU exp2 for a share of the softmax
+    (attention_tc.cu, exp2_fma) stays within 8e-5 relative error of 2^f on
+    [-1/2, 1/2] when evaluated in fp32 Horner form, and the range reduction
+    x = j + f with j = rint(x) reproduces 2^x on the kernel's input range."""
+    import numpy as np
+
+    src = open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", "attention_tc.cu"),
+               encoding="utf-8").read()
+    body = src[src.index("float exp2_fma(float x)"):]
+    body = body[:body.index("}")]
+    coefs = [float(c) for c in re.findall(r"([0-9]\.[0-9]+e[-+][0-9]+)f", body)]
+    assert len(coefs) == 4                      # c3, c2, c1, c0 in Horner order
+    c3, c2, c1, c0 = (np.float32(c) for c in coefs)
+    f = np.linspace(-0.5, 0.5, 200001).astype(np.float32)
+    q = ((c3 * f + c2) * f + c1) * f + c0
+    rel = np.abs(q.astype(np.float64) / np.exp2(f.astype(np.float64)) - 1.0)
+    assert rel.max() < 8e-5
+    # full path on x in [-125, 8]: round to nearest integer via 1.5 * 2^23, scale by 2^j
+    x = np.linspace(-125.0, 8.0, 100001).astype(np.float32)
+    t = (x + np.float32(12582912.0)).astype(np.float32)
+    ff = (x - (t - np.float32(12582912.0))).astype(np.float32)
+    qq = (((c3 * ff + c2) * ff + c1) * ff + c0).astype(np.float32)
+    bits = qq.view(np.int32) + (t.view(np.int32) << 23)
+    y = bits.view(np.float32).astype(np.float64)
+    assert np.all(np.abs(y / np.exp2(x.astype(np.float64)) - 1.0) < 8e-5)
