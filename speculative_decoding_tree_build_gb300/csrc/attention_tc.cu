@@ -121,6 +121,42 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
   const int i0 = blockIdx.x * kRopeNodes;
   if (i0 >= n) return;
   const int i1 = min(n, i0 + kRopeNodes);
+  const bool style0 = p.rope_style == 0;
+  // Work item = one 16-byte vector (8 bf16) of one head of one node; style 0
+  // rotates the pairs inside the vector, style 1 pairs vector v with vector
+  // v + D/16. A thread loads kRopeBatch items before storing any, and the
+  // first batch (every item, for the 8B geometry) is loaded before the
+  // block-table check, so the CTA waits on memory about twice, not five times.
+  constexpr int VPH = D / 8;
+  const int vpn = style0 ? VPH : VPH / 2;
+  const int heads = p.hq + 2 * p.hkv;
+  const int per_node = heads * vpn;
+  const int total = (i1 - i0) * per_node;
+  auto src_of = [&](int idx, int& nd, int& h, int& v) -> const uint4* {
+    nd = idx / per_node;
+    const int rem = idx % per_node;
+    h = rem / vpn;
+    v = rem % vpn;
+    const int t = t0 + i0 + nd;
+    if (h < p.hq) return reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(t) * p.hq + h) * D);
+    if (h < p.hq + p.hkv)
+      return reinterpret_cast<const uint4*>(p.k_new + (static_cast<size_t>(t) * p.hkv + h - p.hq) * D);
+    return reinterpret_cast<const uint4*>(p.v_new + (static_cast<size_t>(t) * p.hkv + h - p.hq - p.hkv) * D);
+  };
+  uint4 xa[kRopeBatch], xb[kRopeBatch];
+  auto load_batch = [&](int base) {
+#pragma unroll
+    for (int u = 0; u < kRopeBatch; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < total) {
+        int nd, h, v;
+        const uint4* src = src_of(idx, nd, h, v);
+        xa[u] = src[v];
+        xb[u] = style0 ? xa[u] : src[v + VPH / 2];
+      }
+    }
+  };
+  load_batch(threadIdx.x);
   // every block holding slots [0, P + n) must be held and in range (the
   // loads of a thread are independent, so they are all in flight at once)
   const long long slots = static_cast<long long>(plen) + n;
@@ -145,39 +181,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
     return;
   }
-  const bool style0 = p.rope_style == 0;
-  // Work item = one 16-byte vector (8 bf16) of one head of one node; style 0
-  // rotates the pairs inside the vector, style 1 pairs vector v with vector
-  // v + D/16. Each thread loads kRopeBatch items before storing any, so the
-  // loads overlap instead of waiting one by one.
-  constexpr int VPH = D / 8;
-  const int vpn = style0 ? VPH : VPH / 2;
-  const int heads = p.hq + 2 * p.hkv;
-  const int per_node = heads * vpn;
-  const int total = (i1 - i0) * per_node;
-  auto src_of = [&](int idx, int& nd, int& h, int& v) -> const uint4* {
-    nd = idx / per_node;
-    const int rem = idx % per_node;
-    h = rem / vpn;
-    v = rem % vpn;
-    const int t = t0 + i0 + nd;
-    if (h < p.hq) return reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(t) * p.hq + h) * D);
-    if (h < p.hq + p.hkv)
-      return reinterpret_cast<const uint4*>(p.k_new + (static_cast<size_t>(t) * p.hkv + h - p.hq) * D);
-    return reinterpret_cast<const uint4*>(p.v_new + (static_cast<size_t>(t) * p.hkv + h - p.hq - p.hkv) * D);
-  };
   for (int base = threadIdx.x; base < total; base += kRopeBatch * blockDim.x) {
-    uint4 xa[kRopeBatch], xb[kRopeBatch];
-#pragma unroll
-    for (int u = 0; u < kRopeBatch; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < total) {
-        int nd, h, v;
-        const uint4* src = src_of(idx, nd, h, v);
-        xa[u] = src[v];
-        xb[u] = style0 ? xa[u] : src[v + VPH / 2];
-      }
-    }
+    if (base != static_cast<int>(threadIdx.x)) load_batch(base);
 #pragma unroll
     for (int u = 0; u < kRopeBatch; ++u) {
       const int idx = base + u * blockDim.x;
