@@ -491,10 +491,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   __shared__ int s_tmp[kTcThreads];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ TcSeg s_last;                // the last segment of this CTA's range (merge task)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
+    s_last.valid = false;
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_empty, 2);
     for (int s = 0; s < kTcStages; ++s) {
@@ -544,6 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     bool ok = true;
     for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
          g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
+      if (lane == 0) s_last = g;
       if (g.skip) continue;
       ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
       if (!ok) break;
@@ -859,11 +862,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // CTA's end, whose first tile is in this range); the merge kernel reads it.
     int32_t* rec = p.tasks + blockIdx.x * kTaskInts;
     int valid = 0;
-    TcSeg last;
-    last.valid = false;
-    for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); g.valid; g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
-      if (s_abort) atomicOr(p.status_rw + g.b, TV_ST_TIMEOUT);   // flag what this CTA touched
-      last = g;
+    const TcSeg last = s_last;            // recorded by the producer as it walked the range
+    if (s_abort) {
+      for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); g.valid; g = tc_segment(p, s_pre, g.t_next, cs, ce))
+        atomicOr(p.status_rw + g.b, TV_ST_TIMEOUT);               // flag what this CTA touched
     }
     if (!s_abort && last.valid && !last.skip && last.tile0 == 0 && last.tile1 < last.ntiles) {
       valid = 1;
