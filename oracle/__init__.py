@@ -20,7 +20,8 @@ Sources (web pages, cited by title and section in each function):
   * "投机解码的树状注意力验证：一次前向如何并行校验多条候选路径" - mask
     correctness rule and tree KV layout / page reclamation;
   * "Accelerating Speculative Decoding with Block Diffusion Draft Trees"
-    (DDTree notes) - flattened tree, position ids and verifier walk (§6, §7).
+    (DDTree notes) - flattened tree, position ids and verifier walk (§6, §7);
+  * "解码：采样、束搜索和推测性解码" - the Gumbel-max sampling trick.
 
 Pinning: every function here is pinned by ``tests/test_oracle_pins.py`` to facts
 that do not come from the oracle itself (printed example values, brute force,
@@ -40,6 +41,7 @@ from .attention_ref import (
 from .accept_ref import greedy_accept_ref, verify_branches_ref
 from .commit_ref import kv_commit_ref
 from .step_ref import verify_step_ref
+from .sample_ref import sample_tokens_ref, sampled_walk_ref
 
 __all__ = [
     "bf16_bits_to_f64", "f64_to_bf16_bits", "round_to_bf16",
@@ -49,5 +51,5 @@ __all__ = [
     "branch_attention_ref", "packed_attention_ref", "dense_tree_mask_ref",
     "gather_prompt_kv_ref", "tree_attention_verify_ref",
     "greedy_accept_ref", "verify_branches_ref", "kv_commit_ref",
-    "verify_step_ref",
+    "verify_step_ref", "sample_tokens_ref", "sampled_walk_ref",
 ]
