@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sampling-steps", type=int, default=200,
+                    help="timed launches of each sampling-acceptance call (0 = skip)")
     return ap.parse_args()
 
 
@@ -90,17 +92,105 @@ def attention_algorithmic(w, depth):
 
 
 def attn_source_sha():
+    return source_sha(ATTN_SOURCES)
+
+
+SAMPLE_SOURCES = ("sample.cu", "tv_common.cuh")
+
+
+def measure_sampling(w, dev, stream, flush, iters, hbm_peak):
+    """Sampling acceptance on the bench workload's trees: per-node target
+    logits over the workload's vocabulary (float32, N(0, 1) with a boosted
+    child token) and float32 Gumbel noise, every request at temperature 1.
+    Times tv_sample_tokens (all nodes) and tv_sampled_accept (the walk, which
+    reads only the visited nodes' rows) with CUDA events, L2 flushed before
+    each launch."""
+    import torch
+
+    import speculative_decoding_tree_build_gb300 as tvb
+    from speculative_decoding_tree_build_gb300 import workloads as wl
+
+    rng = np.random.default_rng(4242 + int(w["config"]))
+    logits_h, gumbel_h = wl.sampling_inputs(rng, w)
+    vocab = int(w["vocab"])
+    bsz = int(w["batch"])
+    total = int(w["cu_nodes"][-1])
+    logits = torch.from_numpy(logits_h).to(dev)
+    gumbel = torch.from_numpy(gumbel_h).to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    cu = torch.from_numpy(np.asarray(w["cu_nodes"], np.int32)).to(dev)
+    parents = torch.from_numpy(np.asarray(w["parents"], np.int32)).to(dev)
+    draft = torch.from_numpy(np.asarray(w["draft_tokens"], np.int32)).to(dev)
+    temps = torch.ones(bsz, dtype=torch.float32, device=dev)
+    status = torch.zeros(bsz, **i32)
+    tokens = torch.empty(total, **i32)
+    md = int(w["max_depth"])
+    path = torch.empty((bsz, md + 1), **i32)
+    alen, bonus = torch.empty(bsz, **i32), torch.empty(bsz, **i32)
+    mn = int(w["max_nodes"])
+
+    def run_sample():
+        tvb.sample_tokens(logits, gumbel, cu, temps, mn, tokens, status, stream)
+
+    def run_walk():
+        tvb.sampled_accept(logits, gumbel, cu, temps, parents, draft, mn, path, alen, bonus,
+                           status, stream)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+
+    us_sample = timed(run_sample)
+    us_walk = timed(run_walk)
+    if int(status.abs().sum()) != 0:
+        raise RuntimeError("sampling produced status flags")
+    visited = int((alen.cpu().numpy() + 1).sum())
+    bytes_sample = total * vocab * 8 + total * 4
+    bytes_walk = visited * vocab * 8
+    gbs_sample = bytes_sample / (us_sample * 1e-6) / 1e9
+    gbs_walk = bytes_walk / (us_walk * 1e-6) / 1e9
+    return {
+        "vocab": vocab, "temperature": 1.0, "nodes": total,
+        "inputs": "float32 logits N(0,1) + boosted child token, float32 Gumbel noise",
+        "sample_tokens": {
+            "us_per_launch": us_sample, "algorithmic_bytes": bytes_sample,
+            "roofline": {"bound": "hbm", "achieved": gbs_sample, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gbs_sample / hbm_peak,
+                         "traffic": recorded_traffic(w["config"], "sample_tokens",
+                                                     SAMPLE_SOURCES)},
+            "nodes_per_s": total / (us_sample * 1e-6)},
+        "sampled_accept": {
+            "us_per_launch": us_walk, "visited_rows": visited, "algorithmic_bytes": bytes_walk,
+            "achieved_gbs": gbs_walk, "frac_of_hbm": gbs_walk / hbm_peak,
+            "speedup_vs_sample_all_then_walk": us_sample / us_walk,
+            "note": "latency-bound: one row per step per request, steps in sequence"},
+    }
+
+
+def source_sha(files):
     h = hashlib.sha256()
-    for f in ATTN_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config):
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current attention source."""
-    path = os.path.join(ROOT, "profiles", f"tree_attention_verify_config{config}.md")
+def recorded_traffic(config, name="tree_attention_verify", sources=ATTN_SOURCES,
+                     key="dram_bytes_per_launch"):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", f"{name}_config{config}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -109,10 +199,10 @@ def recorded_traffic(config):
             if ":" in line and line.startswith("- "):
                 k, v = line[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("attention_source_sha") != attn_source_sha():
+    if vals.get("source_sha", vals.get("attention_source_sha")) != source_sha(sources):
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals[key])
     except (KeyError, ValueError):
         return None
 
@@ -465,10 +555,12 @@ def run_ours(args):
                         "replayed from CUDA graphs",
                 "eager_value": tokens_all / (e2e_eager_ms * 1e-3),
                 "eager_ms_per_step": e2e_eager_ms},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 6 * args.steps,     # tree_build, rope_append, attn_tc, attn_merge, greedy_accept, kv_commit
         "attention_tokens_per_s": tokens_all / (attn_ms * 1e-3),
         "clocks": clocks,
     }
+    if args.sampling_steps > 0:
+        line["sampling"] = measure_sampling(w, dev, stream, flush, args.sampling_steps, hbm_peak)
     if world > 1:
         dist.destroy_process_group()
     if not args.no_cpu_baseline:

@@ -20,6 +20,13 @@
  *   [ATLAS]    "02 · Token Tree 与 Tree Attention"
  *   [WIBLOG]   "投机解码的树状注意力验证：一次前向如何并行校验多条候选路径"
  *   [DDTREE]   "Accelerating Speculative Decoding with Block Diffusion Draft Trees"
+ *   [DECODE]   "解码：采样、束搜索和推测性解码"
+ *
+ * Sampling acceptance (the verifier samples itself, [DDTREE] §7.2-§7.3) adds
+ * two calls that take the target's per-node logits instead of its argmax ids:
+ *
+ *   tv_sample_tokens          the target's sampled (or greedy) token at every node
+ *   tv_sampled_accept         the verifier walk, sampling only the nodes it visits
  *
  * Conventions shared by every call
  * --------------------------------
@@ -71,6 +78,7 @@ extern "C" {
 #define TV_ST_BAD_BLOCK 8          /* a needed block-table entry is missing or out of range */
 #define TV_ST_PATH_OVERFLOW 16     /* accepted path longer than max_depth */
 #define TV_ST_TIMEOUT 32           /* a bounded device wait gave up; that request's outputs are invalid */
+#define TV_ST_BAD_TEMPERATURE 64   /* temperature negative or NaN, or > 0 with no noise array */
 
 #define TV_MAX_NODES 1024          /* largest tree (root included) per request */
 #define TV_BLOCK_SIZE 16
@@ -213,6 +221,67 @@ int tv_greedy_accept(const int32_t* target_ids, const int32_t* draft_tokens,
                      const int32_t* next_sibling, int32_t batch, int32_t max_nodes,
                      int32_t max_depth, int32_t* accept_path, int32_t* accept_len,
                      int32_t* bonus, int32_t* status, void* stream);
+
+/*
+ * Per-node sampling with the Gumbel-max trick ([DECODE] "高效离散采样" /
+ * "Gumbel Max技巧": argmax_v (h_v + g_v) with Gumbel noise g is a draw from
+ * softmax(h); [DDTREE] §7.2: the target picks each node's token with its own
+ * rule, greedy or temperature sampling).
+ *
+ * For node t of request b with temperature T = temperature[b]:
+ *   T == 0: token[t] = first argmax_v logits[t][v]            (greedy)
+ *   T >  0: token[t] = first argmax_v fl(fl(logits[t][v] * fl(1/T)) + gumbel[t][v])
+ * in float32 with each operation rounded (no fused multiply-add). A NaN
+ * counts as the largest value, +0 and -0 tie; ties go to the smallest v.
+ *
+ *  logits         float32 [T][logits_ld], row t holds node t's vocab entries
+ *                 0..vocab-1; 16-byte aligned, logits_ld % 4 == 0, >= vocab
+ *  gumbel         float32 [T][gumbel_ld] noise g = -log(-log(u)), u ~ U(0,1),
+ *                 drawn by the caller; same alignment rules. May be NULL when
+ *                 every temperature is 0 (a request with T > 0 then gets
+ *                 TV_ST_BAD_TEMPERATURE). Not read for greedy requests.
+ *  cu_nodes       int32 [batch+1]
+ *  temperature    float32 [batch] (device)
+ *  max_nodes      largest node count of a request (1..1024)
+ *  vocab          entries per row (1 .. 2^30)
+ *  tokens         int32 [T] out
+ *  status         in/out: requests with non-zero status are skipped;
+ *                 TV_ST_BAD_SIZE (node count > max_nodes) and
+ *                 TV_ST_BAD_TEMPERATURE are OR-ed in (outputs untouched)
+ */
+int tv_sample_tokens(const float* logits, int64_t logits_ld, const float* gumbel,
+                     int64_t gumbel_ld, const int32_t* cu_nodes, const float* temperature,
+                     int32_t batch, int32_t max_nodes, int32_t vocab, int32_t* tokens,
+                     int32_t* status, void* stream);
+
+/*
+ * The verifier walk with the target sampling itself ([DDTREE] §7.2: from the
+ * root, pick a token at the current node with the target's rule; if a child
+ * of the node carries it, move there, else stop with it as the next bonus;
+ * §7.3: the output then follows the target's own autoregressive sampling,
+ * whatever the drafter proposed). The token at a visited node is decided
+ * exactly as tv_sample_tokens decides it, so the result equals
+ * tv_sample_tokens followed by tv_greedy_accept; only the visited nodes'
+ * rows are read (one row of logits, and of noise when sampling, per step).
+ *
+ *  logits, logits_ld, gumbel, gumbel_ld, cu_nodes, temperature, vocab
+ *                 as for tv_sample_tokens
+ *  parents        int32 [T] local parent lists, validated by tv_tree_build
+ *                 (run it first: requests it flagged are skipped)
+ *  draft_tokens   int32 [T]
+ *  max_nodes, max_depth, accept_path, accept_len, bonus
+ *                 as for tv_greedy_accept (among several children carrying
+ *                 the token the smallest index wins)
+ *  status         in/out: requests with non-zero status are skipped;
+ *                 TV_ST_BAD_SIZE, TV_ST_BAD_TEMPERATURE or TV_ST_PATH_OVERFLOW
+ *                 are OR-ed in (outputs untouched)
+ */
+int tv_sampled_accept(const float* logits, int64_t logits_ld, const float* gumbel,
+                      int64_t gumbel_ld, const int32_t* cu_nodes, const float* temperature,
+                      const int32_t* parents, const int32_t* draft_tokens, int32_t batch,
+                      int32_t max_nodes, int32_t max_depth, int32_t vocab,
+                      int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
+                      int32_t* status, void* stream);
 
 /*
  * Commit / rollback of the tentative KV ([GLOSSARY] "Tree/Self Speculation":

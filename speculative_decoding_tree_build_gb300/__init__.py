@@ -17,8 +17,8 @@ import torch
 
 __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
-    "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit", "status_string",
-    "version",
+    "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
+    "sample_tokens", "sampled_accept", "status_string", "version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +26,7 @@ lib_path = os.path.join(_PKG, "libtreeverify.so")
 
 TV_OK = 0
 TV_ST = {"BAD_SIZE": 1, "BAD_ROOT": 2, "BAD_PARENT": 4, "BAD_BLOCK": 8,
-         "PATH_OVERFLOW": 16, "TIMEOUT": 32}
+         "PATH_OVERFLOW": 16, "TIMEOUT": 32, "BAD_TEMPERATURE": 64}
 
 
 class TvGeom(ctypes.Structure):
@@ -46,6 +46,7 @@ _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _SZ = ctypes.c_size_t
+_I64 = ctypes.c_int64
 _SIGS = {
     "tv_workspace_bytes": [ctypes.POINTER(TvGeom), _I, _I, ctypes.POINTER(_SZ)],
     "tv_tree_build": [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -56,6 +57,8 @@ _SIGS = {
     "tv_greedy_accept": [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P],
     "tv_kv_commit": [ctypes.POINTER(TvGeom), _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
                      _P, _P, _P, _P],
+    "tv_sample_tokens": [_P, _I64, _P, _I64, _P, _P, _I, _I, _I, _P, _P, _P],
+    "tv_sampled_accept": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
     "tv_status_string": [ctypes.c_int],
     "tv_version": [],
 }
@@ -192,4 +195,42 @@ def kv_commit(g: TvGeom, accept_path, accept_len, prompt_len, block_table, n_blo
         accept_path.shape[1] - 1, _ptr(prompt_len, I32), _ptr(block_table, I32),
         _ptr(n_blocks, I32), block_table.shape[1], _ptr(k_cache, BF16), _ptr(v_cache, BF16),
         k_cache.shape[0], _ptr(new_len, I32), _ptr(released, I32), _ptr(released_count, I32),
+        _ptr(status, I32), _stream(stream)))
+
+
+def _rows(t, name):
+    """(pointer, row stride) of a float32 [rows][>= vocab] CUDA tensor whose
+    rows are contiguous; None -> (None, 0)."""
+    if t is None:
+        return None, 0
+    if not t.is_cuda or t.dtype != torch.float32 or t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a float32 CUDA matrix with contiguous rows")
+    return t.data_ptr(), t.stride(0)
+
+
+def sample_tokens(logits, gumbel, cu_nodes, temperature, max_nodes, tokens, status, stream=None):
+    """The target's token at every node: greedy (temperature 0) or a
+    Gumbel-max draw. ``logits``/``gumbel`` are [T][vocab] views (row stride
+    may exceed vocab); ``gumbel`` may be None when every temperature is 0."""
+    batch = cu_nodes.numel() - 1
+    lp, lld = _rows(logits, "logits")
+    gp, gld = _rows(gumbel, "gumbel")
+    return _check("tv_sample_tokens", load().tv_sample_tokens(
+        lp, lld, gp, gld, _ptr(cu_nodes, I32, "cu_nodes"),
+        _ptr(temperature, torch.float32, "temperature"), batch, max_nodes, logits.shape[1],
+        _ptr(tokens, I32, "tokens"), _ptr(status, I32, "status"), _stream(stream)))
+
+
+def sampled_accept(logits, gumbel, cu_nodes, temperature, parents, draft_tokens, max_nodes,
+                   accept_path, accept_len, bonus, status, stream=None):
+    """The verifier walk with the target sampling itself at the nodes it
+    visits; same outputs as greedy_accept."""
+    batch = cu_nodes.numel() - 1
+    lp, lld = _rows(logits, "logits")
+    gp, gld = _rows(gumbel, "gumbel")
+    return _check("tv_sampled_accept", load().tv_sampled_accept(
+        lp, lld, gp, gld, _ptr(cu_nodes, I32, "cu_nodes"),
+        _ptr(temperature, torch.float32, "temperature"), _ptr(parents, I32, "parents"),
+        _ptr(draft_tokens, I32, "draft_tokens"), batch, max_nodes, accept_path.shape[1] - 1,
+        logits.shape[1], _ptr(accept_path, I32), _ptr(accept_len, I32), _ptr(bonus, I32),
         _ptr(status, I32), _stream(stream)))

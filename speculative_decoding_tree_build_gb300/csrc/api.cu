@@ -22,7 +22,7 @@ static int check_device() {
 }
 }  // namespace tv
 
-extern "C" int tv_version(void) { return 1; }
+extern "C" int tv_version(void) { return 2; }
 
 extern "C" int tv_workspace_bytes(const tv_geom* geom, int32_t batch, int32_t max_nodes,
                                   size_t* bytes) {
@@ -82,6 +82,7 @@ extern "C" const char* tv_status_string(int code) {
     case TV_ST_BAD_BLOCK: return "TV_ST_BAD_BLOCK";
     case TV_ST_PATH_OVERFLOW: return "TV_ST_PATH_OVERFLOW";
     case TV_ST_TIMEOUT: return "TV_ST_TIMEOUT";
+    case TV_ST_BAD_TEMPERATURE: return "TV_ST_BAD_TEMPERATURE";
     default: return "unknown";
   }
 }

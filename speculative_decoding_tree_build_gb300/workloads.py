@@ -213,6 +213,71 @@ def target_ids_for(rng, parents, tokens, vocab, p_match):
     return tgt
 
 
+def _fill_gumbel(rng, out):
+    """Fill a C-contiguous float32 array with Gumbel(0, 1) draws g = -log(E),
+    E ~ Exp(1) (the same law as -log(-log(u)), u ~ U(0, 1)); E is kept above
+    1e-30 so g stays finite."""
+    rng.standard_exponential(dtype=np.float32, out=out)
+    np.maximum(out, np.float32(1e-30), out=out)
+    np.log(out, out=out)
+    np.negative(out, out=out)
+
+
+def gumbel_noise(rng, shape) -> np.ndarray:
+    """float32 Gumbel(0, 1) noise of the given shape."""
+    out = np.empty(shape, np.float32)
+    _fill_gumbel(rng, out)
+    return out
+
+
+def sampling_inputs(rng, w, vocab=None, sigma=1.0, boost=(8.0, 16.0), ld=None,
+                    pad_value=np.nan):
+    """Per-node target logits and Gumbel noise for the sampled walk.
+
+    logits[t] ~ N(0, sigma) over the vocabulary; with the workload's match
+    probability a node with children gets a uniformly chosen child's token
+    raised by a boost drawn from U(boost), so the sampled token is that child
+    often but not always. Rows have ``ld`` >= vocab columns; the columns past
+    the vocabulary hold ``pad_value`` (NaN by default: a reader that strays
+    there would pick it). Returns (logits, gumbel), float32 [T][ld]."""
+    vocab = w["vocab"] if vocab is None else vocab
+    ld = vocab if ld is None else ld
+    cu = w["cu_nodes"]
+    total = int(cu[-1])
+    logits = np.empty((total, ld), np.float32)
+    gumbel = np.empty((total, ld), np.float32)
+
+    def rows(a):          # C-contiguous pieces covering a[:, :vocab]
+        if ld == vocab:
+            yield a.reshape(-1)
+        else:
+            for r in range(total):
+                yield a[r, :vocab]
+
+    for piece in rows(logits):
+        rng.standard_normal(dtype=np.float32, out=piece)
+        if sigma != 1.0:
+            piece *= np.float32(sigma)
+    for b in range(w["batch"]):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        par = w["parents"][t0:t1]
+        tok = w["draft_tokens"][t0:t1]
+        children = [[] for _ in range(t1 - t0)]
+        for j in range(1, t1 - t0):
+            children[int(par[j])].append(j)
+        for i in range(t1 - t0):
+            if children[i] and rng.random() < w["p_match"]:
+                c = children[i][int(rng.integers(len(children[i])))]
+                if int(tok[c]) < vocab:
+                    logits[t0 + i, int(tok[c])] += np.float32(rng.uniform(*boost))
+    for piece in rows(gumbel):
+        _fill_gumbel(rng, piece)
+    if ld > vocab:
+        logits[:, vocab:] = pad_value
+        gumbel[:, vocab:] = pad_value
+    return logits, gumbel
+
+
 # --------------------------------------------------------------------------
 # batches
 

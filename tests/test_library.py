@@ -33,7 +33,8 @@ def header_functions():
 def test_header_declares_the_step_calls():
     names = header_functions()
     for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
-                 "tv_workspace_bytes", "tv_status_string", "tv_version"):
+                 "tv_sample_tokens", "tv_sampled_accept", "tv_workspace_bytes",
+                 "tv_status_string", "tv_version"):
         assert want in names
 
 
@@ -47,6 +48,7 @@ def test_status_strings(lib):
     assert tv.status_string(0) == "TV_OK"
     assert tv.status_string(-1) == "TV_ERR_NULL_POINTER"
     assert tv.status_string(8) == "TV_ST_BAD_BLOCK"
+    assert tv.status_string(64) == "TV_ST_BAD_TEMPERATURE"
     assert tv.version() >= 1
 
 
@@ -95,6 +97,25 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.tv_tree_attention_verify(ctypes.byref(g), 1, 41, *mis) == -5
     assert L.tv_workspace_bytes(ctypes.byref(bad_d), 1, 41, ctypes.byref(ctypes.c_size_t())) == -2
     assert L.tv_workspace_bytes(ctypes.byref(g), 1, 41, None) == -1
+    # sampling: (logits, ld, gumbel, ld, cu, temperature, batch, max_nodes, vocab, tokens, status)
+    S = L.tv_sample_tokens
+    assert S(P, 32000, P, 32000, P, P, 0, 8, 32000, P, P, None) == 0
+    assert S(P, 32000, P, 32000, P, P, -1, 8, 32000, P, P, None) == -3
+    assert S(P, 32000, P, 32000, P, P, 1, 1025, 32000, P, P, None) == -3
+    assert S(P, 32000, P, 32000, P, P, 1, 8, 0, P, P, None) == -3
+    assert S(P, 100, P, 32000, P, P, 1, 8, 32000, P, P, None) == -3     # ld < vocab
+    assert S(P, 32000, P, 100, P, P, 1, 8, 32000, P, P, None) == -3
+    assert S(None, 32000, P, 32000, P, P, 1, 8, 32000, P, P, None) == -1
+    assert S(P, 32000, P, 32000, P, None, 1, 8, 32000, P, P, None) == -1
+    assert S(P + 4, 32000, P, 32000, P, P, 1, 8, 32000, P, P, None) == -5
+    assert S(P, 32002, P, 32000, P, P, 1, 8, 32000, P, P, None) == -5   # row stride % 4
+    assert S(P, 32000, P + 8, 32000, P, P, 1, 8, 32000, P, P, None) == -5
+    A = L.tv_sampled_accept
+    args = [P, 32000, P, 32000, P, P, P, P, 1, 8, 4, 32000, P, P, P, P, None]
+    assert A(*args[:8], 0, *args[9:]) == 0
+    assert A(*args[:10], -1, *args[11:]) == -3                          # max_depth
+    assert A(*args[:6], None, *args[7:]) == -1                          # parents
+    assert A(P + 4, *args[1:]) == -5
 
 
 def test_fma_exp2_cubic_error_bound():
