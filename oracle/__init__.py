@@ -42,6 +42,7 @@ from .accept_ref import greedy_accept_ref, verify_branches_ref
 from .commit_ref import kv_commit_ref
 from .step_ref import verify_step_ref
 from .sample_ref import sample_tokens_ref, sampled_walk_ref
+from .ddtree_ref import ddtree_build_ref, ddtree_from_logits_ref, topk_logprobs_ref
 
 __all__ = [
     "bf16_bits_to_f64", "f64_to_bf16_bits", "round_to_bf16",
@@ -52,4 +53,5 @@ __all__ = [
     "gather_prompt_kv_ref", "tree_attention_verify_ref",
     "greedy_accept_ref", "verify_branches_ref", "kv_commit_ref",
     "verify_step_ref", "sample_tokens_ref", "sampled_walk_ref",
+    "topk_logprobs_ref", "ddtree_build_ref", "ddtree_from_logits_ref",
 ]
