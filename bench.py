@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sampling-steps", type=int, default=200,
-                    help="timed launches of each sampling-acceptance call (0 = skip)")
+                    help="timed launches of each sampling-acceptance and DDTree-construction "
+                         "call (0 = skip)")
     return ap.parse_args()
 
 
@@ -96,6 +97,73 @@ def attn_source_sha():
 
 
 SAMPLE_SOURCES = ("sample.cu", "tv_common.cuh")
+
+
+DDTREE_SOURCES = ("ddtree.cu", "tv_common.cuh")
+
+
+def measure_ddtree(dev, stream, flush, iters, hbm_peak):
+    """DDTree draft-tree construction with the DDTree workload's drafter
+    recipe: 16 requests x L = 16 positions, vocabulary 151936, logits
+    N(0, 3) (float32), budget B = 256 (K = 256). Times tv_ddtree_topk (HBM:
+    every logit read once) and tv_ddtree_build (B dependent heap pops per
+    request) with CUDA events, L2 flushed before each launch."""
+    import torch
+
+    import speculative_decoding_tree_build_gb300 as tvb
+
+    batch, L, V, B = 16, 16, 151936, 256
+    rng = np.random.default_rng(4004)
+    logits_h = np.empty((batch * L, V), np.float32)
+    rng.standard_normal(dtype=np.float32, out=logits_h)
+    logits_h *= np.float32(3.0)
+    logits = torch.from_numpy(logits_h).to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    tt = torch.empty((batch * L, B), **i32)
+    tq = torch.empty((batch * L, B), dtype=torch.float32, device=dev)
+    n = tvb.ddtree_nodes(L, B, B)
+    par, tok = torch.empty(batch * n, **i32), torch.empty(batch * n, **i32)
+    cu = torch.empty(batch + 1, **i32)
+
+    def run_topk():
+        tvb.ddtree_topk(logits, B, tt, tq, stream)
+
+    def run_build():
+        tvb.ddtree_build(tq.view(batch, L, B), tt.view(batch, L, B), B, par, tok, cu,
+                         stream=stream)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+
+    us_topk = timed(run_topk)
+    us_build = timed(run_build)
+    nbytes = batch * L * V * 4 + batch * L * B * 8
+    gbs = nbytes / (us_topk * 1e-6) / 1e9
+    return {
+        "workload": "16 requests x 16 positions, vocabulary 151936, N(0,3) float32 logits, B=256",
+        "ddtree_topk": {"us_per_launch": us_topk, "algorithmic_bytes": nbytes,
+                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": gbs / hbm_peak,
+                                     "traffic": recorded_traffic(4, "ddtree_topk",
+                                                                 DDTREE_SOURCES)}},
+        "ddtree_build": {"us_per_launch": us_build, "pops_per_request": B,
+                         "ns_per_pop": us_build * 1e3 / B,
+                         "note": "latency-bound: B dependent best-first pops per request, "
+                                 "one warp per request, all requests in parallel"},
+        "trees_per_s": batch / ((us_topk + us_build) * 1e-6),
+    }
 
 
 def measure_sampling(w, dev, stream, flush, iters, hbm_peak):
@@ -561,6 +629,8 @@ def run_ours(args):
     }
     if args.sampling_steps > 0:
         line["sampling"] = measure_sampling(w, dev, stream, flush, args.sampling_steps, hbm_peak)
+        line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps,
+                                                     hbm_peak)
     if world > 1:
         dist.destroy_process_group()
     if not args.no_cpu_baseline:

@@ -28,6 +28,12 @@
  *   tv_sample_tokens          the target's sampled (or greedy) token at every node
  *   tv_sampled_accept         the verifier walk, sampling only the nodes it visits
  *
+ * Draft-tree construction ([DDTREE] §4-§5) builds the tree that tv_tree_build
+ * consumes from a block drafter's per-position logits:
+ *
+ *   tv_ddtree_topk            per position: top-K tokens and log-probabilities
+ *   tv_ddtree_build           best-first heap (Algorithm 1) -> parent lists
+ *
  * Conventions shared by every call
  * --------------------------------
  *  - All array arguments are DEVICE pointers owned by the caller. The library
@@ -282,6 +288,58 @@ int tv_sampled_accept(const float* logits, int64_t logits_ld, const float* gumbe
                       int32_t max_nodes, int32_t max_depth, int32_t vocab,
                       int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
                       int32_t* status, void* stream);
+
+/*
+ * Nodes (root included) of the trees tv_ddtree_build makes: 1 + min(budget,
+ * sum_{d=1..L} k^d). Returns that count, or TV_ERR_BAD_SIZE when depth_L < 1,
+ * k < 1 or budget outside [1, 1023].
+ */
+int tv_ddtree_nodes(int32_t depth_L, int32_t k, int32_t budget);
+
+/*
+ * Per-position top-K of a block drafter's logits ([DDTREE] §4.3, Lemma 1:
+ * only each depth's top K = min(B, |V|) tokens can enter the optimal tree;
+ * §3-§4.1: q_i = softmax of position i's logits).
+ *
+ *  logits         float32 [rows][logits_ld], row r holds vocab logits;
+ *                 16-byte aligned, logits_ld % 4 == 0, logits_ld >= vocab.
+ *                 Rows of a batch of requests with L positions each are
+ *                 row = request * L + position. Logits must not be NaN; -inf
+ *                 is allowed (a row with no finite logit gets log q = -inf).
+ *  vocab          entries per row (1 .. 2^30), k in [1, min(vocab, 1024)]
+ *  top_tokens     int32 [rows][k] out  tokens by logit descending, equal
+ *                 logits by token id ascending
+ *  top_logq       float32 [rows][k] out  log softmax(row)[token]: the logit
+ *                 minus the row's log-sum-exp (accumulated in float32 per
+ *                 thread, combined in float64; absolute error about 1e-6)
+ */
+int tv_ddtree_topk(const float* logits, int64_t logits_ld, int32_t rows, int32_t vocab,
+                   int32_t k, int32_t* top_tokens, float* top_logq, void* stream);
+
+/*
+ * DDTree best-first construction ([DDTREE] §5, Algorithm 1; §4.2,
+ * Proposition 2: the budget most probable prefixes form a prefix-closed,
+ * optimal tree; §6-§7.1: flattened depth by depth after the root).
+ *
+ *  top_logq       float32 [batch][depth_L][k], top_tokens int32 [batch][depth_L][k]:
+ *                 per depth, the k candidates in rank order (tv_ddtree_topk)
+ *  budget         prefixes to select, 1..1023; every tree gets
+ *                 n = tv_ddtree_nodes(depth_L, k, budget) nodes
+ *  root_tokens    int32 [batch] token of each root (the previous bonus), or
+ *                 NULL for -1
+ *  parents        int32 [batch * n] out  local parent index, -1 for the root
+ *  tokens         int32 [batch * n] out
+ *  cu_nodes       int32 [batch + 1] out  b * n
+ * A prefix's score is its parent's score plus its own log-probability, added
+ * in float32; equal scores take the shallower prefix, then the one whose
+ * parent was selected first. Nodes are ordered root first, then by depth,
+ * selection order within a depth, so parents precede children and the
+ * output feeds tv_tree_build directly. Shared memory: 4 L k + 20 n bytes
+ * (at most 200 KB, else TV_ERR_BAD_SIZE).
+ */
+int tv_ddtree_build(const float* top_logq, const int32_t* top_tokens, int32_t batch,
+                    int32_t depth_L, int32_t k, int32_t budget, const int32_t* root_tokens,
+                    int32_t* parents, int32_t* tokens, int32_t* cu_nodes, void* stream);
 
 /*
  * Commit / rollback of the tentative KV ([GLOSSARY] "Tree/Self Speculation":

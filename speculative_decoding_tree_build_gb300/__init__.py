@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
     "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
-    "sample_tokens", "sampled_accept", "status_string", "version",
+    "sample_tokens", "sampled_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
+    "status_string", "version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -59,6 +60,9 @@ _SIGS = {
                      _P, _P, _P, _P],
     "tv_sample_tokens": [_P, _I64, _P, _I64, _P, _P, _I, _I, _I, _P, _P, _P],
     "tv_sampled_accept": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
+    "tv_ddtree_nodes": [_I, _I, _I],
+    "tv_ddtree_topk": [_P, _I64, _I, _I, _I, _P, _P, _P],
+    "tv_ddtree_build": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
     "tv_status_string": [ctypes.c_int],
     "tv_version": [],
 }
@@ -234,3 +238,33 @@ def sampled_accept(logits, gumbel, cu_nodes, temperature, parents, draft_tokens,
         _ptr(draft_tokens, I32, "draft_tokens"), batch, max_nodes, accept_path.shape[1] - 1,
         logits.shape[1], _ptr(accept_path, I32), _ptr(accept_len, I32), _ptr(bonus, I32),
         _ptr(status, I32), _stream(stream)))
+
+
+def ddtree_nodes(depth_L: int, k: int, budget: int) -> int:
+    """Nodes (root included) of every tree tv_ddtree_build makes for these sizes."""
+    n = load().tv_ddtree_nodes(depth_L, k, budget)
+    if n < 0:
+        raise TvError("tv_ddtree_nodes", n)
+    return n
+
+
+def ddtree_topk(logits, k, top_tokens, top_logq, stream=None):
+    """Per row of ``logits`` ([rows][vocab] view with contiguous rows): the k
+    most probable tokens (logit descending, token ascending) and their
+    log-probabilities."""
+    lp, lld = _rows(logits, "logits")
+    return _check("tv_ddtree_topk", load().tv_ddtree_topk(
+        lp, lld, logits.shape[0], logits.shape[1], k, _ptr(top_tokens, I32, "top_tokens"),
+        _ptr(top_logq, torch.float32, "top_logq"), _stream(stream)))
+
+
+def ddtree_build(top_logq, top_tokens, budget, parents, tokens, cu_nodes, root_tokens=None,
+                 stream=None):
+    """DDTree best-first construction from per-depth top-K log-probabilities
+    ``top_logq`` / ``top_tokens`` of shape [batch][L][k]; writes the flattened
+    trees (root first, depth by depth) and their node offsets."""
+    batch, depth_l, k = top_logq.shape
+    return _check("tv_ddtree_build", load().tv_ddtree_build(
+        _ptr(top_logq, torch.float32, "top_logq"), _ptr(top_tokens, I32, "top_tokens"), batch,
+        depth_l, k, budget, _ptr(root_tokens, I32, "root_tokens"), _ptr(parents, I32, "parents"),
+        _ptr(tokens, I32, "tokens"), _ptr(cu_nodes, I32, "cu_nodes"), _stream(stream)))

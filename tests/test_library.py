@@ -33,7 +33,8 @@ def header_functions():
 def test_header_declares_the_step_calls():
     names = header_functions()
     for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
-                 "tv_sample_tokens", "tv_sampled_accept", "tv_workspace_bytes",
+                 "tv_sample_tokens", "tv_sampled_accept", "tv_ddtree_topk", "tv_ddtree_build",
+                 "tv_ddtree_nodes", "tv_workspace_bytes",
                  "tv_status_string", "tv_version"):
         assert want in names
 
@@ -116,6 +117,23 @@ def test_host_validation_rejects_before_launch(lib):
     assert A(*args[:10], -1, *args[11:]) == -3                          # max_depth
     assert A(*args[:6], None, *args[7:]) == -1                          # parents
     assert A(P + 4, *args[1:]) == -5
+    # DDTree construction
+    assert L.tv_ddtree_nodes(16, 256, 256) == 257
+    assert L.tv_ddtree_nodes(3, 4, 6) == 7 and L.tv_ddtree_nodes(4, 2, 100) == 31
+    assert L.tv_ddtree_nodes(0, 4, 6) == -3 and L.tv_ddtree_nodes(3, 4, 1024) == -3
+    T = L.tv_ddtree_topk
+    assert T(P, 1000, 0, 1000, 8, P, P, None) == 0
+    assert T(P, 1000, 4, 1000, 1001, P, P, None) == -3      # k > vocab
+    assert T(P, 2000, 4, 2000, 1025, P, P, None) == -3      # k > 1024
+    assert T(P, 999, 4, 1000, 8, P, P, None) == -3          # ld < vocab
+    assert T(None, 1000, 4, 1000, 8, P, P, None) == -1
+    assert T(P + 4, 1000, 4, 1000, 8, P, P, None) == -5
+    assert T(P, 1002, 4, 1000, 8, P, P, None) == -5
+    Bd = L.tv_ddtree_build
+    assert Bd(P, P, 0, 16, 256, 256, None, P, P, P, None) == 0
+    assert Bd(P, P, 2, 16, 256, 1024, None, P, P, P, None) == -3
+    assert Bd(P, P, 2, 64, 1023, 1023, None, P, P, P, None) == -3   # shared memory too large
+    assert Bd(P, None, 2, 16, 256, 256, None, P, P, P, None) == -1
 
 
 def test_fma_exp2_cubic_error_bound():
