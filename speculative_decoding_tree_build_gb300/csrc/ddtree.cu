@@ -244,22 +244,32 @@ ddtree_topk_kernel(const float* __restrict__ logits, long long ld, int vocab, in
       s = acc;
       m = nm;
     }
-    // admission (warp-aggregated); most warps skip it once tau has risen
+    // admission: one warp scan of the admitted counts, one atomic per warp;
+    // most warps skip it once tau has risen
     if (__any_sync(0xffffffffu, cm >= tau)) {
+      uint32_t amask = 0;
 #pragma unroll
       for (int e = 0; e < kTopkVec * 4; ++e) {
         const int i = base + (tid + (e >> 2) * kTopkThreads) * 4 + (e & 3);
-        const bool in = i < vocab && x[e] >= tau;
-        const uint32_t msk = __ballot_sync(0xffffffffu, in);
-        if (msk) {
-          int slot = 0;
-          if (lane == __ffs(msk) - 1) slot = atomicAdd(&sh.count, __popc(msk));
-          slot = __shfl_sync(0xffffffffu, slot, __ffs(msk) - 1);
-          if (in) {
-            const uint64_t key = cand_key(x[e], i);
-            buf[slot + __popc(msk & ((1u << lane) - 1u))] = key;
-            atomicAdd(&hist[key_bin(key)], 1u);
-          }
+        if (i < vocab && x[e] >= tau) amask |= 1u << e;
+      }
+      const int cnt = __popc(amask);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int slot = 0;
+      if (lane == 31 && incl > 0) slot = atomicAdd(&sh.count, incl);
+      slot = __shfl_sync(0xffffffffu, slot, 31) + incl - cnt;
+#pragma unroll
+      for (int e = 0; e < kTopkVec * 4; ++e) {
+        if (amask & (1u << e)) {
+          const int i = base + (tid + (e >> 2) * kTopkThreads) * 4 + (e & 3);
+          const uint64_t key = cand_key(x[e], i);
+          buf[slot++] = key;
+          atomicAdd(&hist[key_bin(key)], 1u);
         }
       }
     }
