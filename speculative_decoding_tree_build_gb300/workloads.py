@@ -86,7 +86,7 @@ def _topk_logprobs(rng, vocab, k, sigma):
 
 
 def eagle_tree(rng, depth, topk, keep, vocab, sigma=2.0, until_count=False,
-               max_layers=32):
+               max_layers=32, return_candidates=False):
     """EAGLE-2 style dynamic tree.
 
     Layer 1 is the root's top-k children; layer l expands the top-k nodes of
@@ -95,7 +95,9 @@ def eagle_tree(rng, depth, topk, keep, vocab, sigma=2.0, until_count=False,
     (at most ``max_layers``) instead of exactly ``depth`` layers. The global
     top-``keep`` candidates by cumulative score are kept (prefix-closed because
     every child scores strictly below its parent) and packed in BFS order.
-    Returns (parents, tokens, scores) with node 0 the root.
+    Returns (parents, tokens, scores) with node 0 the root; with
+    ``return_candidates`` also (logp, parent, token) of every generated
+    candidate in generation order (parent -1 for the root's children).
     """
     # candidate: (score, depth, gen, parent_gen, rank, token)
     cands = []
@@ -138,7 +140,37 @@ def eagle_tree(rng, depth, topk, keep, vocab, sigma=2.0, until_count=False,
     parents = [-1] + [packed_of[c[3]] for c in order]
     tokens = [0] + [c[5] for c in order]
     scores = [0.0] + [c[0] for c in order]
-    return np.array(parents, np.int32), np.array(tokens, np.int32), np.array(scores)
+    out = (np.array(parents, np.int32), np.array(tokens, np.int32), np.array(scores))
+    if return_candidates:
+        logp = np.array([c[0] - (cands[c[3]][0] if c[3] >= 0 else 0.0) for c in cands])
+        out += ((logp, np.array([c[3] for c in cands], np.int32),
+                 np.array([c[5] for c in cands], np.int32)),)
+    return out
+
+
+def eagle_candidates(rng, layers, topk, vocab, sigma=2.0, chooser=None):
+    """Candidates of an EAGLE-style expansion, in generation order: layer 1 is
+    the root's top-k children (drafter log-probs from log_softmax of N(0,
+    sigma) logits); each later layer gives top-k children to the layer nodes
+    named by ``chooser(logp, parent, layer)`` (default: the first topk nodes
+    of the layer, generation order). Returns (logp float32, parent, token)."""
+    logp, parent, token = [], [], []
+    toks, lps = _topk_logprobs(rng, vocab, topk, sigma)
+    layer_nodes = []
+    for r in range(topk):
+        layer_nodes.append(len(logp))
+        logp.append(lps[r]); parent.append(-1); token.append(int(toks[r]))
+    for lay in range(1, layers):
+        lp = np.array(logp, np.float32)
+        par = np.array(parent, np.int32)
+        chosen = chooser(lp, par, lay) if chooser is not None else layer_nodes[:topk]
+        layer_nodes = []
+        for pc in chosen:
+            toks, lps = _topk_logprobs(rng, vocab, topk, sigma)
+            for r in range(topk):
+                layer_nodes.append(len(logp))
+                logp.append(lps[r]); parent.append(int(pc)); token.append(int(toks[r]))
+    return (np.array(logp, np.float32), np.array(parent, np.int32), np.array(token, np.int32))
 
 
 def ddtree_marginals(rng, length, vocab, sigma=3.0, k=None):
