@@ -102,6 +102,63 @@ SAMPLE_SOURCES = ("sample.cu", "tv_common.cuh")
 DDTREE_SOURCES = ("ddtree.cu", "tv_common.cuh")
 
 
+def measure_eagle(dev, stream, flush, iters):
+    """EAGLE-2 selection with the EAGLE-2 workload's recipe: 32 requests, six
+    layers of top-8 expansion (328 candidates each; drafter log-probs from
+    log_softmax of N(0, 2) logits), global top 64. Times one layer's
+    tv_eagle_expand_select and tv_eagle_rerank (CUDA events, L2 flushed)."""
+    import torch
+
+    import speculative_decoding_tree_build_gb300 as tvb
+    from speculative_decoding_tree_build_gb300 import workloads as wl
+
+    rng = np.random.default_rng(3003)
+    batch, layers, k, keep = 32, 6, 8, 64
+    reqs = [wl.eagle_candidates(rng, layers, k, 32000, 2.0) for _ in range(batch)]
+    m = max(len(r[0]) for r in reqs)
+    lp = np.zeros((batch, m), np.float32)
+    par = np.full((batch, m), -1, np.int32)
+    tok = np.zeros((batch, m), np.int32)
+    cnt = np.zeros(batch, np.int32)
+    for i, (l, p, t) in enumerate(reqs):
+        lp[i, :len(l)], par[i, :len(l)], tok[i, :len(l)], cnt[i] = l, p, t, len(l)
+    i32 = dict(dtype=torch.int32, device=dev)
+    d_lp, d_par, d_tok, d_cnt = (torch.from_numpy(a).to(dev) for a in (lp, par, tok, cnt))
+    sel = torch.empty((batch, k), **i32)
+    st = torch.zeros(batch, **i32)
+    parents = torch.empty(batch * (keep + 1), **i32)
+    tokens = torch.empty(batch * (keep + 1), **i32)
+    cu = torch.empty(batch + 1, **i32)
+
+    def run_select():
+        tvb.eagle_expand_select(d_lp, d_par, d_cnt, layers - 1, k, sel, st, stream)
+
+    def run_rerank():
+        tvb.eagle_rerank(d_lp, d_par, d_tok, d_cnt, keep, parents, tokens, cu, st, stream=stream)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+
+    us_sel, us_rr = timed(run_select), timed(run_rerank)
+    if int(st.abs().sum()) != 0:
+        raise RuntimeError("EAGLE selection produced status flags")
+    return {"workload": f"32 requests, {m} candidates each (6 layers x top-8), keep 64",
+            "expand_select_us": us_sel, "rerank_us": us_rr,
+            "note": "latency-bound: one CTA per request, candidates ranked in shared memory"}
+
+
 def measure_ddtree(dev, stream, flush, iters, hbm_peak):
     """DDTree draft-tree construction with the DDTree workload's drafter
     recipe: 16 requests x L = 16 positions, vocabulary 151936, logits
@@ -631,6 +688,7 @@ def run_ours(args):
         line["sampling"] = measure_sampling(w, dev, stream, flush, args.sampling_steps, hbm_peak)
         line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps,
                                                      hbm_peak)
+        line["eagle_selection"] = measure_eagle(dev, stream, flush, args.sampling_steps)
     if world > 1:
         dist.destroy_process_group()
     if not args.no_cpu_baseline:

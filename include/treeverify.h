@@ -34,6 +34,12 @@
  *   tv_ddtree_topk            per position: top-K tokens and log-probabilities
  *   tv_ddtree_build           best-first heap (Algorithm 1) -> parent lists
  *
+ * EAGLE-2 dynamic trees ([ATLAS] §3, §5) are selected from a drafter's
+ * layer-by-layer candidates:
+ *
+ *   tv_eagle_expand_select    per layer: the top-k candidates to expand next
+ *   tv_eagle_rerank           global top-N by survival probability -> parent lists
+ *
  * Conventions shared by every call
  * --------------------------------
  *  - All array arguments are DEVICE pointers owned by the caller. The library
@@ -340,6 +346,49 @@ int tv_ddtree_topk(const float* logits, int64_t logits_ld, int32_t rows, int32_t
 int tv_ddtree_build(const float* top_logq, const int32_t* top_tokens, int32_t batch,
                     int32_t depth_L, int32_t k, int32_t budget, const int32_t* root_tokens,
                     int32_t* parents, int32_t* tokens, int32_t* cu_nodes, void* stream);
+
+/*
+ * Candidates of an EAGLE-style expansion, shared by the two calls below.
+ * Request b owns candidates [b * max_cands, b * max_cands + cand_count[b]) in
+ * generation order (a parent before its children):
+ *  logp     float32  drafter log-probability of the candidate's token under
+ *                    its parent (<= 0)
+ *  parent   int32    index of the parent candidate within the request, -1 for
+ *                    the root's children (TV_ST_BAD_PARENT if outside [-1, c))
+ *  token    int32
+ * A candidate's score is its parent's score plus its own log-probability
+ * (float32, in that order) - the log of its prefix survival probability;
+ * its depth is its parent's plus one (root's children: 1). max_cands <= 4096.
+ */
+
+/*
+ * Layer expansion ([ATLAS] §3: each step expands the top-k nodes of the
+ * current layer): the k candidates of depth `layer` with the largest scores,
+ * earlier generated first on ties.
+ *  selected   int32 [batch][k] out  candidate indices, best first, -1 when the
+ *             layer has fewer than k candidates
+ *  status     in/out: requests with non-zero status are skipped
+ */
+int tv_eagle_expand_select(const float* logp, const int32_t* parent, const int32_t* cand_count,
+                           int32_t batch, int32_t max_cands, int32_t layer, int32_t k,
+                           int32_t* selected, int32_t* status, void* stream);
+
+/*
+ * Global rerank ([ATLAS] §5: EAGLE-2 keeps the N_tree nodes with the largest
+ * prefix survival probability): the n_keep best candidates (score
+ * descending, then shallower, then earlier generated), packed breadth first
+ * (depth, parent's packed index, generation order) after the root.
+ *  root_tokens  int32 [batch] or NULL (-1)
+ *  parents, tokens  int32 [batch * (n_keep + 1)] out; cu_nodes int32 [batch + 1] out
+ *  status     in/out: requests with non-zero status are skipped; TV_ST_BAD_SIZE
+ *             when cand_count < n_keep or the kept set is not prefix-closed
+ *             (a positive log-probability), TV_ST_BAD_PARENT (outputs untouched)
+ * n_keep in [1, 1023].
+ */
+int tv_eagle_rerank(const float* logp, const int32_t* parent, const int32_t* token,
+                    const int32_t* cand_count, int32_t batch, int32_t max_cands, int32_t n_keep,
+                    const int32_t* root_tokens, int32_t* parents, int32_t* tokens,
+                    int32_t* cu_nodes, int32_t* status, void* stream);
 
 /*
  * Commit / rollback of the tentative KV ([GLOSSARY] "Tree/Self Speculation":

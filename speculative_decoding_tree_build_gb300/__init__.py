@@ -19,7 +19,7 @@ __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
     "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
     "sample_tokens", "sampled_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
-    "status_string", "version",
+    "eagle_expand_select", "eagle_rerank", "status_string", "version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +63,8 @@ _SIGS = {
     "tv_ddtree_nodes": [_I, _I, _I],
     "tv_ddtree_topk": [_P, _I64, _I, _I, _I, _P, _P, _P],
     "tv_ddtree_build": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
+    "tv_eagle_expand_select": [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P],
+    "tv_eagle_rerank": [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "tv_status_string": [ctypes.c_int],
     "tv_version": [],
 }
@@ -268,3 +270,25 @@ def ddtree_build(top_logq, top_tokens, budget, parents, tokens, cu_nodes, root_t
         _ptr(top_logq, torch.float32, "top_logq"), _ptr(top_tokens, I32, "top_tokens"), batch,
         depth_l, k, budget, _ptr(root_tokens, I32, "root_tokens"), _ptr(parents, I32, "parents"),
         _ptr(tokens, I32, "tokens"), _ptr(cu_nodes, I32, "cu_nodes"), _stream(stream)))
+
+
+def eagle_expand_select(logp, parent, cand_count, layer, k, selected, status, stream=None):
+    """Top-k candidates of depth ``layer`` per request. ``logp``/``parent``
+    are [batch][max_cands] (generation order), ``selected`` [batch][k]."""
+    batch, max_cands = logp.shape
+    return _check("tv_eagle_expand_select", load().tv_eagle_expand_select(
+        _ptr(logp, torch.float32, "logp"), _ptr(parent, I32, "parent"),
+        _ptr(cand_count, I32, "cand_count"), batch, max_cands, layer, k,
+        _ptr(selected, I32, "selected"), _ptr(status, I32, "status"), _stream(stream)))
+
+
+def eagle_rerank(logp, parent, token, cand_count, n_keep, parents, tokens, cu_nodes, status,
+                 root_tokens=None, stream=None):
+    """Global top-``n_keep`` candidates per request, packed breadth first."""
+    batch, max_cands = logp.shape
+    return _check("tv_eagle_rerank", load().tv_eagle_rerank(
+        _ptr(logp, torch.float32, "logp"), _ptr(parent, I32, "parent"), _ptr(token, I32, "token"),
+        _ptr(cand_count, I32, "cand_count"), batch, max_cands, n_keep,
+        _ptr(root_tokens, I32, "root_tokens"), _ptr(parents, I32, "parents"),
+        _ptr(tokens, I32, "tokens"), _ptr(cu_nodes, I32, "cu_nodes"), _ptr(status, I32, "status"),
+        _stream(stream)))

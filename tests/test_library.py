@@ -34,7 +34,8 @@ def test_header_declares_the_step_calls():
     names = header_functions()
     for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
                  "tv_sample_tokens", "tv_sampled_accept", "tv_ddtree_topk", "tv_ddtree_build",
-                 "tv_ddtree_nodes", "tv_workspace_bytes",
+                 "tv_ddtree_nodes", "tv_eagle_expand_select", "tv_eagle_rerank",
+                 "tv_workspace_bytes",
                  "tv_status_string", "tv_version"):
         assert want in names
 
@@ -134,6 +135,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert Bd(P, P, 2, 16, 256, 1024, None, P, P, P, None) == -3
     assert Bd(P, P, 2, 64, 1023, 1023, None, P, P, P, None) == -3   # shared memory too large
     assert Bd(P, None, 2, 16, 256, 256, None, P, P, P, None) == -1
+    # EAGLE-2 selection
+    E = L.tv_eagle_expand_select
+    assert E(P, P, P, 0, 400, 1, 8, P, P, None) == 0
+    assert E(P, P, P, 2, 4097, 1, 8, P, P, None) == -3
+    assert E(P, P, P, 2, 400, 0, 8, P, P, None) == -3
+    assert E(P, None, P, 2, 400, 1, 8, P, P, None) == -1
+    R = L.tv_eagle_rerank
+    assert R(P, P, P, P, 0, 400, 64, None, P, P, P, P, None) == 0
+    assert R(P, P, P, P, 2, 400, 1024, None, P, P, P, P, None) == -3
+    assert R(P, P, P, P, 2, 40, 64, None, P, P, P, P, None) == -3     # n_keep > max_cands
+    assert R(P, P, None, P, 2, 400, 64, None, P, P, P, P, None) == -1
 
 
 def test_fma_exp2_cubic_error_bound():
