@@ -102,6 +102,42 @@ SAMPLE_SOURCES = ("sample.cu", "tv_common.cuh")
 DDTREE_SOURCES = ("ddtree.cu", "tv_common.cuh")
 
 
+def measure_dense_mask(w, db, stream, flush, iters, hbm_peak):
+    """Dense FULL_MASK export of the bench workload's trees (bool and additive
+    float32), write-bound; CUDA events, L2 flushed before each launch."""
+    import torch
+
+    import speculative_decoding_tree_build_gb300 as tvb
+
+    n_el = tvb.dense_mask_elements(w["cu_nodes"], w["prompt_len"], tvb.MASK_FULL)
+    res = {}
+    for name, dt, tdt, size in (("bool", tvb.MASK_BOOL, torch.uint8, 1),
+                                ("additive_f32", tvb.MASK_ADDITIVE_F32, torch.float32, 4)):
+        out = torch.empty(n_el, dtype=tdt, device=db.mask.device)
+        st = torch.zeros_like(db.status)
+
+        def fn():
+            tvb.tree_mask_dense(db.mask, db.cu_nodes, db.prompt_len, st, int(w["max_nodes"]), out,
+                                tvb.MASK_FULL, dt, stream)
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+        gbs = n_el * size / (us * 1e-6) / 1e9
+        res[name] = {"us_per_launch": us, "bytes_written": n_el * size, "achieved_gbs": gbs,
+                     "frac_of_hbm": gbs / hbm_peak}
+    return res
+
+
 def measure_eagle(dev, stream, flush, iters):
     """EAGLE-2 selection with the EAGLE-2 workload's recipe: 32 requests, six
     layers of top-8 expansion (328 candidates each; drafter log-probs from
@@ -689,6 +725,8 @@ def run_ours(args):
         line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps,
                                                      hbm_peak)
         line["eagle_selection"] = measure_eagle(dev, stream, flush, args.sampling_steps)
+        line["dense_mask_export"] = measure_dense_mask(w, db, stream, flush, args.sampling_steps,
+                                                       hbm_peak)
     if world > 1:
         dist.destroy_process_group()
     if not args.no_cpu_baseline:

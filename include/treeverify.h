@@ -7,7 +7,8 @@
  *
  *   tv_tree_build             parent list -> bit-packed ancestor mask, depth
  *                             positions, retrieve_index / next_token /
- *                             next_sibling
+ *                             next_sibling (tv_tree_mask_dense exports the
+ *                             mask densely for other attention code)
  *   tv_tree_attention_verify  depth-RoPE of the tree's fresh Q/K, tentative KV
  *                             write, GQA attention over the paged prompt cache
  *                             plus each node's ancestors
@@ -140,6 +141,30 @@ int tv_tree_build(const int32_t* parents, const int32_t* cu_nodes, const int32_t
                   int32_t batch, int32_t max_nodes, uint32_t* mask_bits, int32_t* depth,
                   int32_t* positions, int32_t* retrieve_index, int32_t* next_token,
                   int32_t* next_sibling, int32_t* status, void* stream);
+
+/*
+ * Dense export of the tree mask ([GLOSSARY] "Packed tree attention": the
+ * [N, P+N] mask, bool or additive -inf, in which a node sees the whole prefix
+ * plus its ancestor chain and itself; [ATLAS] §3: the FULL_MASK and QLEN_ONLY
+ * modes beside bit-packing), for attention code that takes a dense mask.
+ *
+ *  mask_bits, cu_nodes, prompt_len, max_nodes   as for tv_tree_build
+ *  status     int32 [batch] in: requests with non-zero status are not written
+ *  mode       TV_MASK_FULL: request b's block is [N_b][P_b + N_b] (prompt
+ *             columns first); TV_MASK_QLEN_ONLY: [N_b][N_b] (tree columns only)
+ *  dtype      TV_MASK_BOOL: uint8, 1 visible / 0 masked;
+ *             TV_MASK_ADDITIVE_F32: float32, 0 visible / -inf masked
+ *             (out 4-byte aligned)
+ *  out        the requests' blocks back to back, row-major, no padding:
+ *             sum_b N_b (max(P_b, 0) + N_b) elements (FULL), sum_b N_b^2 (QLEN_ONLY)
+ */
+#define TV_MASK_FULL 0
+#define TV_MASK_QLEN_ONLY 1
+#define TV_MASK_BOOL 0
+#define TV_MASK_ADDITIVE_F32 1
+int tv_tree_mask_dense(const uint32_t* mask_bits, const int32_t* cu_nodes,
+                       const int32_t* prompt_len, const int32_t* status, int32_t batch,
+                       int32_t max_nodes, int32_t mode, int32_t dtype, void* out, void* stream);
 
 /*
  * Packed tree attention with depth RoPE and the tentative KV write

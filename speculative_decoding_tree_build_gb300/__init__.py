@@ -19,7 +19,8 @@ __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
     "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
     "sample_tokens", "sampled_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
-    "eagle_expand_select", "eagle_rerank", "status_string", "version",
+    "eagle_expand_select", "eagle_rerank", "tree_mask_dense", "dense_mask_elements",
+    "status_string", "version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +66,7 @@ _SIGS = {
     "tv_ddtree_build": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
     "tv_eagle_expand_select": [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P],
     "tv_eagle_rerank": [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P],
+    "tv_tree_mask_dense": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
     "tv_status_string": [ctypes.c_int],
     "tv_version": [],
 }
@@ -292,3 +294,31 @@ def eagle_rerank(logp, parent, token, cand_count, n_keep, parents, tokens, cu_no
         _ptr(root_tokens, I32, "root_tokens"), _ptr(parents, I32, "parents"),
         _ptr(tokens, I32, "tokens"), _ptr(cu_nodes, I32, "cu_nodes"), _ptr(status, I32, "status"),
         _stream(stream)))
+
+
+MASK_FULL, MASK_QLEN_ONLY = 0, 1
+MASK_BOOL, MASK_ADDITIVE_F32 = 0, 1
+
+
+def dense_mask_elements(cu_nodes, prompt_len, mode=MASK_FULL) -> int:
+    """Elements tv_tree_mask_dense writes (host arrays or tensors)."""
+    import numpy as np
+    cu = np.asarray(cu_nodes.cpu() if hasattr(cu_nodes, "cpu") else cu_nodes, np.int64)
+    n = np.diff(cu)
+    if mode == MASK_QLEN_ONLY:
+        return int(np.sum(n * n))
+    p = np.maximum(np.asarray(prompt_len.cpu() if hasattr(prompt_len, "cpu") else prompt_len,
+                              np.int64), 0)
+    return int(np.sum(n * (p + n)))
+
+
+def tree_mask_dense(mask_bits, cu_nodes, prompt_len, status, max_nodes, out, mode=MASK_FULL,
+                    dtype=MASK_BOOL, stream=None):
+    """Dense [N, P+N] (or [N, N]) masks of all requests, back to back in
+    ``out`` (uint8 for MASK_BOOL, float32 for MASK_ADDITIVE_F32)."""
+    want = torch.uint8 if dtype == MASK_BOOL else torch.float32
+    batch = cu_nodes.numel() - 1
+    return _check("tv_tree_mask_dense", load().tv_tree_mask_dense(
+        _ptr(mask_bits, None, "mask_bits"), _ptr(cu_nodes, I32, "cu_nodes"),
+        _ptr(prompt_len, I32, "prompt_len"), _ptr(status, I32, "status"), batch, max_nodes,
+        mode, dtype, _ptr(out, want, "out"), _stream(stream)))
