@@ -547,8 +547,7 @@ def run_ours(args):
     w = wl.make_config(args.config, seed=1000 + args.config + 7919 * rank)
     db = DeviceBatch(w, device=dev)
     stream = torch.cuda.current_stream(dev)
-    table0 = db.block_table.clone()
-    nblk0 = db.n_blocks.clone()
+    table0 = db.table_state.clone()          # block table + block counts, one buffer
     tokens_per_step = int(w["cu_nodes"][-1])
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int32, device=dev)
@@ -567,13 +566,11 @@ def run_ours(args):
     flush = _Flush()
 
     def pre():
-        db.block_table.copy_(table0, non_blocking=True)   # allocator refill
-        db.n_blocks.copy_(nblk0, non_blocking=True)
+        db.table_state.copy_(table0, non_blocking=True)   # allocator refill
         db.tree_build()
 
     def post():
-        db.accept()
-        db.commit()
+        db.accept_commit()                   # greedy_accept + kv_commit, one kernel
 
     def step():
         pre()
@@ -726,7 +723,7 @@ def run_ours(args):
                         "replayed from CUDA graphs",
                 "eager_value": tokens_all / (e2e_eager_ms * 1e-3),
                 "eager_ms_per_step": e2e_eager_ms},
-        "gpu_launches": 6 * args.steps,     # tree_build, rope_append, attn_tc, attn_merge, greedy_accept, kv_commit
+        "gpu_launches": 5 * args.steps,     # tree_build, rope_append, attn_tc, attn_merge, accept_commit
         "attention_tokens_per_s": tokens_all / (attn_ms * 1e-3),
         "clocks": clocks,
     }

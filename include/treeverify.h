@@ -443,6 +443,21 @@ int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* accept_path,
                  void* k_cache, void* v_cache, int32_t num_blocks, int32_t* new_len,
                  int32_t* released, int32_t* released_count, int32_t* status, void* stream);
 
+/*
+ * tv_greedy_accept followed by tv_kv_commit in one kernel launch (the
+ * accepted path stays on chip between the two): the union of their arguments
+ * (max_depth is the path capacity, accept_path rows hold max_depth + 1
+ * entries), the same outputs and status flags as the two calls in sequence.
+ */
+int tv_accept_commit(const tv_geom* geom, const int32_t* target_ids, const int32_t* draft_tokens,
+                     const int32_t* cu_nodes, const int32_t* next_token,
+                     const int32_t* next_sibling, int32_t batch, int32_t max_nodes,
+                     int32_t max_depth, int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
+                     const int32_t* prompt_len, int32_t* block_table, int32_t* n_blocks,
+                     int32_t max_blocks_per_req, void* k_cache, void* v_cache, int32_t num_blocks,
+                     int32_t* new_len, int32_t* released, int32_t* released_count,
+                     int32_t* status, void* stream);
+
 /* Name of a TV_ERR_* code or of a single TV_ST_* flag. */
 const char* tv_status_string(int code);
 

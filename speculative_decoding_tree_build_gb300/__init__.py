@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
     "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
+    "accept_commit",
     "sample_tokens", "sampled_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
     "eagle_expand_select", "eagle_rerank", "tree_mask_dense", "dense_mask_elements",
     "status_string", "version",
@@ -67,6 +68,8 @@ _SIGS = {
     "tv_eagle_expand_select": [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P],
     "tv_eagle_rerank": [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "tv_tree_mask_dense": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
+    "tv_accept_commit": [ctypes.POINTER(TvGeom), _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P,
+                         _P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _P],
     "tv_status_string": [ctypes.c_int],
     "tv_version": [],
 }
@@ -322,3 +325,17 @@ def tree_mask_dense(mask_bits, cu_nodes, prompt_len, status, max_nodes, out, mod
         _ptr(mask_bits, None, "mask_bits"), _ptr(cu_nodes, I32, "cu_nodes"),
         _ptr(prompt_len, I32, "prompt_len"), _ptr(status, I32, "status"), batch, max_nodes,
         mode, dtype, _ptr(out, want, "out"), _stream(stream)))
+
+
+def accept_commit(g: TvGeom, target_ids, draft_tokens, cu_nodes, next_token, next_sibling,
+                  max_nodes, accept_path, accept_len, bonus, prompt_len, block_table, n_blocks,
+                  k_cache, v_cache, new_len, released, released_count, status, stream=None):
+    """greedy_accept followed by kv_commit in one kernel (same outputs)."""
+    batch = cu_nodes.numel() - 1
+    return _check("tv_accept_commit", load().tv_accept_commit(
+        ctypes.byref(g), _ptr(target_ids, I32, "target_ids"), _ptr(draft_tokens, I32, "draft_tokens"),
+        _ptr(cu_nodes, I32), _ptr(next_token, I32), _ptr(next_sibling, I32), batch, max_nodes,
+        accept_path.shape[1] - 1, _ptr(accept_path, I32), _ptr(accept_len, I32), _ptr(bonus, I32),
+        _ptr(prompt_len, I32), _ptr(block_table, I32), _ptr(n_blocks, I32), block_table.shape[1],
+        _ptr(k_cache, BF16), _ptr(v_cache, BF16), k_cache.shape[0], _ptr(new_len, I32),
+        _ptr(released, I32), _ptr(released_count, I32), _ptr(status, I32), _stream(stream)))

@@ -22,7 +22,7 @@ static int check_device() {
 }
 }  // namespace tv
 
-extern "C" int tv_version(void) { return 3; }
+extern "C" int tv_version(void) { return 4; }
 
 extern "C" int tv_workspace_bytes(const tv_geom* geom, int32_t batch, int32_t max_nodes,
                                   size_t* bytes) {

@@ -12,7 +12,7 @@
 // One CTA per request: the request's arrays are staged into shared memory
 // with coalesced loads, then one thread walks first-child / next-sibling links
 // there (shared-memory latency instead of a chain of dependent global loads).
-#include "tv_common.cuh"
+#include "tv_step.cuh"
 
 namespace tv {
 
@@ -25,12 +25,7 @@ greedy_accept_kernel(const int32_t* __restrict__ target_ids,
                      const int32_t* __restrict__ next_sibling, int max_nodes, int max_depth,
                      int32_t* __restrict__ accept_path, int32_t* __restrict__ accept_len,
                      int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
-  __shared__ int s_tgt[TV_MAX_NODES];
-  __shared__ int s_tok[TV_MAX_NODES];
-  __shared__ int s_first[TV_MAX_NODES];
-  __shared__ int s_next[TV_MAX_NODES];
-  __shared__ int s_path[TV_MAX_NODES];
-  __shared__ int s_len, s_bonus, s_bad;
+  __shared__ WalkSmem w;
   grid_dependency_wait();                 // inputs written by the previous kernel are visible
   grid_launch_dependents();
   const int b = blockIdx.x;
@@ -42,48 +37,17 @@ greedy_accept_kernel(const int32_t* __restrict__ target_ids,
     if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
     return;
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    s_tgt[i] = target_ids[t0 + i];
-    s_tok[i] = draft_tokens[t0 + i];
-    s_first[i] = next_token[t0 + i];
-    s_next[i] = next_sibling[t0 + i];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int len = 0, cur = 0, bad = 0;
-    s_path[0] = 0;
-    while (true) {
-      const int want = s_tgt[cur];
-      int c = s_first[cur];
-      int guard = 0;
-      while (c != -1 && s_tok[c] != want) {
-        c = s_next[c];
-        // links come from tv_tree_build; a corrupted list must not loop or
-        // index outside the request
-        if (c >= n || c < -1 || ++guard > n) { bad = 1; break; }
-      }
-      if (bad || c == -1) {
-        s_bonus = want;
-        break;
-      }
-      if (c <= cur || c >= n || len + 1 >= n) { bad = 1; break; }
-      s_path[++len] = c;
-      cur = c;
-    }
-    s_len = len;
-    s_bad = bad ? TV_ST_BAD_SIZE : (len > max_depth ? TV_ST_PATH_OVERFLOW : 0);
-  }
-  __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) atomicOr(&status[b], s_bad);
+  greedy_walk(target_ids, draft_tokens, next_token, next_sibling, t0, n, max_depth, w);
+  if (w.bad) {
+    if (threadIdx.x == 0) atomicOr(&status[b], w.bad);
     return;
   }
-  const int len = s_len;
+  const int len = w.len;
   int32_t* row = accept_path + static_cast<size_t>(b) * (max_depth + 1);
-  for (int k = threadIdx.x; k <= max_depth; k += blockDim.x) row[k] = k <= len ? s_path[k] : -1;
+  for (int k = threadIdx.x; k <= max_depth; k += blockDim.x) row[k] = k <= len ? w.path[k] : -1;
   if (threadIdx.x == 0) {
     accept_len[b] = len;
-    bonus[b] = s_bonus;
+    bonus[b] = w.bonus;
   }
 }
 

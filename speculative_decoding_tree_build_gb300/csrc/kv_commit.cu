@@ -14,7 +14,7 @@
 // therefore moved in ascending chunks, each chunk staged in shared memory
 // (all of its reads before any of its writes); later chunks only read slots
 // that no earlier chunk wrote. One CTA per request; byte moves are exact.
-#include "tv_common.cuh"
+#include "tv_step.cuh"
 
 namespace tv {
 
@@ -32,7 +32,7 @@ kv_commit_kernel(const int32_t* __restrict__ accept_path, const int32_t* __restr
   extern __shared__ uint4 stage[];
   __shared__ int s_path[TV_MAX_NODES];
   __shared__ int s_blk[2 * TV_MAX_NODES];
-  __shared__ int s_bad;
+  __shared__ int s_flag;
   grid_dependency_wait();                 // inputs written by the previous kernel are visible
   grid_launch_dependents();
   const int b = blockIdx.x;
@@ -44,88 +44,18 @@ kv_commit_kernel(const int32_t* __restrict__ accept_path, const int32_t* __restr
   const int held = n_blocks[b];
   const int32_t* path = accept_path + static_cast<size_t>(b) * (max_depth + 1);
   for (int k = threadIdx.x; k <= max_depth && k < TV_MAX_NODES; k += blockDim.x) s_path[k] = path[k];
-  if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   if (st != 0) return;
   if (a < 0 || a > max_depth || a >= TV_MAX_NODES || plen < 0 || held < 0 || held > max_blocks) {
     if (threadIdx.x == 0) atomicOr(&status[b], TV_ST_BAD_SIZE);
     return;
   }
-  const int32_t* table = block_table + static_cast<size_t>(b) * max_blocks;
-  int bad = 0;
-  for (int k = threadIdx.x; k <= a; k += blockDim.x) {
-    const int pk = s_path[k];
-    if (k == 0) {
-      if (pk != 0) bad |= TV_ST_BAD_SIZE;
-      continue;
-    }
-    if (pk <= s_path[k - 1]) { bad |= TV_ST_BAD_SIZE; continue; }
-    // source and destination blocks of row k
-    const long long src = static_cast<long long>(plen) + pk, dst = plen + k;
-    const long long lbs = src / TV_BLOCK_SIZE, lbd = dst / TV_BLOCK_SIZE;
-    int bs = -1, bd = -1;
-    if (lbs < held && lbs < max_blocks) bs = table[lbs];
-    if (lbd < held && lbd < max_blocks) bd = table[lbd];
-    if (bs < 0 || bs >= num_blocks || bd < 0 || bd >= num_blocks) bad |= TV_ST_BAD_BLOCK;
-    s_blk[2 * k] = bs;
-    s_blk[2 * k + 1] = bd;
-  }
-  if (bad) atomicOr(&s_bad, bad);
-  __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) atomicOr(&status[b], s_bad);
-    return;
-  }
-
-  // rows to move (skip k with path[k] == k: already in place)
-  const int row_vecs = 2 * hkv * head_vecs;   // K and V, all heads
-  const int chunk_rows = kCommitSmem / (row_vecs * 16);
-  for (int k0 = 1; k0 <= a; k0 += chunk_rows) {
-    const int k1 = min(a + 1, k0 + chunk_rows);
-    const int total = (k1 - k0) * row_vecs;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-      const int r = e / row_vecs, rem = e % row_vecs;
-      const int k = k0 + r;
-      if (s_path[k] == k) continue;
-      const int kv = rem / (hkv * head_vecs), h = (rem / head_vecs) % hkv, v = rem % head_vecs;
-      const int slot = (plen + s_path[k]) % TV_BLOCK_SIZE;
-      const size_t idx = ((static_cast<size_t>(s_blk[2 * k]) * hkv + h) * TV_BLOCK_SIZE + slot) *
-                             head_vecs + v;
-      stage[e] = kv ? v_cache[idx] : k_cache[idx];
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-      const int r = e / row_vecs, rem = e % row_vecs;
-      const int k = k0 + r;
-      if (s_path[k] == k) continue;
-      const int kv = rem / (hkv * head_vecs), h = (rem / head_vecs) % hkv, v = rem % head_vecs;
-      const int slot = (plen + k) % TV_BLOCK_SIZE;
-      const size_t idx = ((static_cast<size_t>(s_blk[2 * k + 1]) * hkv + h) * TV_BLOCK_SIZE + slot) *
-                             head_vecs + v;
-      if (kv) v_cache[idx] = stage[e]; else k_cache[idx] = stage[e];
-    }
-    __syncthreads();
-  }
-
-  // release the blocks past the new end
-  const long long nl = static_cast<long long>(plen) + 1 + a;
-  const int keep = static_cast<int>((nl + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
-  const int count = held > keep ? held - keep : 0;
-  int32_t* trow = block_table + static_cast<size_t>(b) * max_blocks;
-  int32_t* rrow = released + static_cast<size_t>(b) * max_blocks;
-  for (int j = threadIdx.x; j < max_blocks; j += blockDim.x) {
-    if (j < count && keep + j < max_blocks) {
-      rrow[j] = trow[keep + j];
-      trow[keep + j] = -1;
-    } else {
-      rrow[j] = -1;
-    }
-  }
-  if (threadIdx.x == 0) {
-    new_len[b] = static_cast<int>(nl);
-    released_count[b] = count;
-    n_blocks[b] = held < keep ? held : keep;
-  }
+  const int flag = commit_rows(s_path, a, plen, held, block_table + static_cast<size_t>(b) * max_blocks,
+                               max_blocks, k_cache, v_cache, num_blocks, hkv, head_vecs, stage,
+                               kCommitSmem, s_blk, &s_flag, &new_len[b],
+                               released + static_cast<size_t>(b) * max_blocks, &released_count[b],
+                               &n_blocks[b]);
+  if (flag && threadIdx.x == 0) atomicOr(&status[b], flag);
 }
 
 }  // namespace tv

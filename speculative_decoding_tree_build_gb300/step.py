@@ -7,8 +7,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (geom as make_geom, greedy_accept, kv_commit, tree_attention_verify, tree_build,
-               workspace_bytes)
+from . import (accept_commit, geom as make_geom, greedy_accept, kv_commit, tree_attention_verify,
+               tree_build, workspace_bytes)
 
 _STEP_INPUTS = ("parents", "cu_nodes", "prompt_len", "draft_tokens", "target_ids")
 
@@ -37,8 +37,13 @@ class DeviceBatch:
         self.batch = int(w["batch"])
         self.k_cache = _bf16(w["k_cache"], dev)
         self.v_cache = _bf16(w["v_cache"], dev)
-        self.block_table = _i32(w["block_table"], dev)
-        self.n_blocks = _i32(w["n_blocks"], dev)
+        # block table and per-request block counts share one buffer, so an
+        # allocator can save or restore both with one copy
+        table = np.ascontiguousarray(w["block_table"], dtype=np.int32)
+        nblk = np.ascontiguousarray(w["n_blocks"], dtype=np.int32)
+        self.table_state = _i32(np.concatenate([table.reshape(-1), nblk]), dev)
+        self.block_table = self.table_state[:table.size].view(table.shape)
+        self.n_blocks = self.table_state[table.size:]
         self.load_step_inputs(w)
         ws = workspace_bytes(self.g, self.batch, self.max_nodes)
         if workspace is None:
@@ -96,6 +101,14 @@ class DeviceBatch:
         kv_commit(self.g, self.accept_path, self.accept_len, self.prompt_len, self.block_table,
                   self.n_blocks, self.k_cache, self.v_cache, self.new_len, self.released,
                   self.released_count, self.status, stream)
+
+    def accept_commit(self, stream=None):
+        """accept + commit fused into one kernel (tv_accept_commit)."""
+        accept_commit(self.g, self.target_ids, self.draft_tokens, self.cu_nodes, self.next_token,
+                      self.next_sibling, self.max_nodes, self.accept_path, self.accept_len,
+                      self.bonus, self.prompt_len, self.block_table, self.n_blocks, self.k_cache,
+                      self.v_cache, self.new_len, self.released, self.released_count, self.status,
+                      stream)
 
     def step(self, stream=None):
         self.tree_build(stream)

@@ -105,7 +105,7 @@ def run_gpu(w, calls=("build", "attn", "accept", "commit"), db=None):
     db = db or DeviceBatch(w)
     for c in calls:
         {"build": db.tree_build, "attn": db.attention, "accept": db.accept,
-         "commit": db.commit}[c]()
+         "commit": db.commit, "accept_commit": db.accept_commit}[c]()
     torch.cuda.synchronize()
     return db
 

@@ -73,10 +73,10 @@ def _check_step(w, db_pre_k, db_pre_v, db, ref, pairs=None):
         assert np.all(rel[b][cnt[b]:] == -1)
 
 
-def _run_and_check(w, pairs=None):
+def _run_and_check(w, pairs=None, fused=False):
     db = run_gpu(w, ("build", "attn"))
     pre_k, pre_v = db.cache_bits()
-    run_gpu(w, ("accept", "commit"), db)
+    run_gpu(w, ("accept_commit",) if fused else ("accept", "commit"), db)
     ref = oracle_step(w, sample=pairs)
     _check_step(w, pre_k, pre_v, db, ref, pairs)
     return db, ref
@@ -86,6 +86,13 @@ def _run_and_check(w, pairs=None):
 def test_step_small_all_outputs(cfg):
     w = wl.make_config(cfg, **SMALL[cfg])
     _run_and_check(w)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_step_small_fused_accept_commit(cfg):
+    """tv_accept_commit against the same oracle step as the two calls."""
+    w = wl.make_config(cfg, **SMALL[cfg])
+    _run_and_check(w, fused=True)
 
 
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])

@@ -35,7 +35,7 @@ def test_header_declares_the_step_calls():
     for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
                  "tv_sample_tokens", "tv_sampled_accept", "tv_ddtree_topk", "tv_ddtree_build",
                  "tv_ddtree_nodes", "tv_eagle_expand_select", "tv_eagle_rerank",
-                 "tv_tree_mask_dense",
+                 "tv_tree_mask_dense", "tv_accept_commit",
                  "tv_workspace_bytes",
                  "tv_status_string", "tv_version"):
         assert want in names
@@ -147,6 +147,16 @@ def test_host_validation_rejects_before_launch(lib):
     assert R(P, P, P, P, 2, 400, 1024, None, P, P, P, P, None) == -3
     assert R(P, P, P, P, 2, 40, 64, None, P, P, P, P, None) == -3     # n_keep > max_cands
     assert R(P, P, None, P, 2, 400, 64, None, P, P, P, P, None) == -1
+    # fused accept + commit
+    AC = L.tv_accept_commit
+    assert AC(ctypes.byref(g), P, P, P, P, P, 0, 41, 4, P, P, P, P, P, P, 8, P, P, 10, P, P, P, P,
+              None) == 0
+    assert AC(ctypes.byref(bad_d), P, P, P, P, P, 1, 41, 4, P, P, P, P, P, P, 8, P, P, 10, P, P, P,
+              P, None) == -2
+    assert AC(ctypes.byref(g), P, P, P, P, P, 1, 41, -1, P, P, P, P, P, P, 8, P, P, 10, P, P, P, P,
+              None) == -3
+    assert AC(ctypes.byref(g), P, None, P, P, P, 1, 41, 4, P, P, P, P, P, P, 8, P, P, 10, P, P, P,
+              P, None) == -1
     # dense mask export
     M = L.tv_tree_mask_dense
     assert M(P, P, P, P, 0, 41, 0, 0, P, None) == 0
