@@ -490,6 +490,26 @@ def cpu_baseline(w, seconds):
                       f"{wall:.1f} s wall"}
 
 
+def rank_seed(config, rank):
+    """Each rank verifies its own batch (requests are independent)."""
+    return 1000 + config + 7919 * rank
+
+
+def reduce_over_ranks(times_ms, tokens, world, device):
+    """Whole-job numbers of a weak-scaling run: every time is the maximum over
+    ranks (the job ends with its slowest rank), the token count the sum."""
+    import torch
+    import torch.distributed as dist
+
+    if world <= 1:
+        return [float(t) for t in times_ms], float(tokens)
+    mx = torch.tensor([float(t) for t in times_ms], dtype=torch.float64, device=device)
+    sm = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return [float(t) for t in mx.tolist()], float(sm[0])
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -544,7 +564,7 @@ def run_ours(args):
     from speculative_decoding_tree_build_gb300 import workloads as wl
     from speculative_decoding_tree_build_gb300.step import DeviceBatch
 
-    w = wl.make_config(args.config, seed=1000 + args.config + 7919 * rank)
+    w = wl.make_config(args.config, seed=rank_seed(args.config, rank))
     db = DeviceBatch(w, device=dev)
     stream = torch.cuda.current_stream(dev)
     table0 = db.table_state.clone()          # block table + block counts, one buffer
@@ -676,17 +696,8 @@ def run_ours(args):
     e2e_ms = e2e_loop(graph_step)          # host buffers in/out, graph-replayed API calls
     e2e_eager_ms = e2e_loop(step)          # host buffers in/out, one Python call per API entry
 
-    vals = torch.tensor([step_ms, attn_ms, e2e_ms, float(tokens_per_step)], dtype=torch.float64,
-                        device=dev)
-    if world > 1:
-        mx = vals.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = vals.clone()
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        step_ms, attn_ms, e2e_ms = float(mx[0]), float(mx[1]), float(mx[2])
-        tokens_all = float(sm[3])
-    else:
-        tokens_all = float(tokens_per_step)
+    (step_ms, attn_ms, e2e_ms), tokens_all = reduce_over_ranks(
+        [step_ms, attn_ms, e2e_ms], tokens_per_step, world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
