@@ -13,6 +13,19 @@ from . import (accept_commit, geom as make_geom, greedy_accept, kv_commit, tree_
 _STEP_INPUTS = ("parents", "cu_nodes", "prompt_len", "draft_tokens", "target_ids")
 
 
+def _arena(specs, dev):
+    """One device buffer holding several tensors back to back (16-byte
+    aligned): (buffer, {name: view}). specs: [(name, shape, dtype)]."""
+    offs, off = {}, 0
+    for name, shape, dtype in specs:
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        offs[name] = (off, shape, dtype, nbytes)
+        off += -(-nbytes // 16) * 16
+    buf = torch.zeros(max(off, 16), dtype=torch.uint8, device=dev)
+    views = {name: buf[o:o + n].view(dtype).view(shape) for name, (o, shape, dtype, n) in offs.items()}
+    return buf, views
+
+
 def _i32(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
@@ -49,26 +62,34 @@ class DeviceBatch:
         if workspace is None:
             workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
         self.workspace = workspace
-        self.status = torch.zeros(self.batch, dtype=torch.int32, device=dev)
-        self.accept_path = torch.zeros(self.batch, self.max_depth + 1, dtype=torch.int32, device=dev)
-        self.accept_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
-        self.bonus = torch.zeros(self.batch, dtype=torch.int32, device=dev)
-        self.new_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
-        self.released = torch.zeros(self.batch, self.block_table.shape[1], dtype=torch.int32, device=dev)
-        self.released_count = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        # the step's results live in one buffer too (one device-to-host copy)
+        bsz, mb = self.batch, self.block_table.shape[1]
+        self.outputs, views = _arena([
+            ("status", (bsz,), torch.int32), ("accept_path", (bsz, self.max_depth + 1), torch.int32),
+            ("accept_len", (bsz,), torch.int32), ("bonus", (bsz,), torch.int32),
+            ("new_len", (bsz,), torch.int32), ("released", (bsz, mb), torch.int32),
+            ("released_count", (bsz,), torch.int32)], dev)
+        for name, t in views.items():
+            setattr(self, name, t)
 
     def load_step_inputs(self, w):
         """(Re)load the per-step inputs (tree, tokens, fresh Q/K/V) and size
-        the per-node outputs."""
+        the per-node outputs. The inputs share one device buffer, so a caller
+        feeding them from the host needs one copy per step."""
         dev = self.device
-        self.parents = _i32(w["parents"], dev)
-        self.cu_nodes = _i32(w["cu_nodes"], dev)
-        self.prompt_len = _i32(w["prompt_len"], dev)
-        self.draft_tokens = _i32(w["draft_tokens"], dev)
-        self.target_ids = _i32(w["target_ids"], dev)
-        self.q = _bf16(w["q"], dev)
-        self.k_new = _bf16(w["k_new"], dev)
-        self.v_new = _bf16(w["v_new"], dev)
+        total = int(w["cu_nodes"][-1])
+        hq, hkv, d = w["num_q_heads"], w["num_kv_heads"], w["head_dim"]
+        specs = [("parents", (total,), torch.int32), ("cu_nodes", (self.batch + 1,), torch.int32),
+                 ("prompt_len", (self.batch,), torch.int32), ("draft_tokens", (total,), torch.int32),
+                 ("target_ids", (total,), torch.int32), ("q", (total, hq, d), torch.bfloat16),
+                 ("k_new", (total, hkv, d), torch.bfloat16), ("v_new", (total, hkv, d), torch.bfloat16)]
+        self.inputs, views = _arena(specs, dev)
+        for name, t in views.items():
+            setattr(self, name, t)
+        for name in ("parents", "cu_nodes", "prompt_len", "draft_tokens", "target_ids"):
+            getattr(self, name).copy_(_i32(w[name], dev))
+        for name in ("q", "k_new", "v_new"):
+            getattr(self, name).copy_(_bf16(w[name], dev).view(getattr(self, name).shape))
         total = int(w["cu_nodes"][-1])
         words = (self.max_nodes + 31) // 32
         self.mask = torch.zeros(total, words, dtype=torch.int32, device=dev)
