@@ -193,3 +193,9 @@ def test_fma_exp2_cubic_error_bound():
     bits = qq.view(np.int32) + (t.view(np.int32) << 23)
     y = bits.view(np.float32).astype(np.float64)
     assert np.all(np.abs(y / np.exp2(x.astype(np.float64)) - 1.0) < 8e-5)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: without the built library the binding raises."""
+    with pytest.raises(FileNotFoundError):
+        tv.load(str(tmp_path / "libtreeverify.so"))
