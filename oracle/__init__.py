@@ -44,6 +44,7 @@ from .step_ref import verify_step_ref
 from .sample_ref import sample_tokens_ref, sampled_walk_ref
 from .ddtree_ref import ddtree_build_ref, ddtree_from_logits_ref, topk_logprobs_ref
 from .eagle_ref import eagle_expand_select_ref, eagle_rerank_ref, eagle_scores_ref
+from .rejection_ref import chosen_path_ref, rejection_walk_ref
 
 __all__ = [
     "bf16_bits_to_f64", "f64_to_bf16_bits", "round_to_bf16",
@@ -56,4 +57,5 @@ __all__ = [
     "verify_step_ref", "sample_tokens_ref", "sampled_walk_ref",
     "topk_logprobs_ref", "ddtree_build_ref", "ddtree_from_logits_ref",
     "eagle_scores_ref", "eagle_expand_select_ref", "eagle_rerank_ref",
+    "chosen_path_ref", "rejection_walk_ref",
 ]
