@@ -29,6 +29,11 @@
  *   tv_sample_tokens          the target's sampled (or greedy) token at every node
  *   tv_sampled_accept         the verifier walk, sampling only the nodes it visits
  *
+ * Rejection-sampling acceptance ([ATLAS] §4: one chosen path accepted edge by
+ * edge with the min(1, p/q) rule) takes the drafter's logits as well:
+ *
+ *   tv_rejection_accept       chosen path, per-edge acceptance, correction draw
+ *
  * Draft-tree construction ([DDTREE] §4-§5) builds the tree that tv_tree_build
  * consumes from a block drafter's per-position logits:
  *
@@ -319,6 +324,63 @@ int tv_sampled_accept(const float* logits, int64_t logits_ld, const float* gumbe
                       int32_t max_nodes, int32_t max_depth, int32_t vocab,
                       int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
                       int32_t* status, void* stream);
+
+/*
+ * Rejection-sampling verification along one chosen path ([ATLAS] §4: the
+ * target's logits at every node come from the one forward; one best path is
+ * chosen by its log-probability and accepted from the root edge by edge with
+ * the min(1, p/q) rule; a rejection ends the walk with a correction token
+ * sampled at the current node, a fully accepted path with the bonus token
+ * sampled at its last node; [DECODE] "Gumbel Max技巧" for the draws).
+ *
+ * For request b with temperature T = temperature[b]:
+ *   path   root to the leaf with the largest sum of draft_logp over its nodes
+ *          (float64 sums, node 0 contributes 0; the smallest leaf index on ties)
+ *   p_u    softmax(logits[u] / T) (T == 0: all mass on the first argmax)
+ *   q_u    softmax(draft_logits[u]), the distribution u's children were drawn from
+ *   edge u -> c on the path is accepted when uniforms[c] < p_u(x_c) / q_u(x_c),
+ *          x_c = draft_tokens[c] (q_u(x_c) == 0 accepts; x_c outside
+ *          [0, vocab) rejects); the first rejection at u stops the walk
+ *   bonus  after a rejection at u: Gumbel-max draw over max(0, p_u - q_u)
+ *          (over p_u when that is zero everywhere) with noise row gumbel[u];
+ *          after the whole path: draw over p at the last node; T == 0: the
+ *          first argmax of the stop node's logits.
+ * Log-sum-exps are reduced in float32 and finished in float64; the per-edge
+ * ratios in float64; the residual keys log(p_v - q_v) + g_v in float32. A
+ * decision can therefore differ from an exact evaluation only where the
+ * exact margin is within float32 rounding.
+ *
+ *  logits, logits_ld   float32 [T][logits_ld] target logits, row per node
+ *                      (logits_ld >= vocab)
+ *  draft_logits, draft_ld
+ *                      float32 [T][draft_ld] drafter logits at each node
+ *  gumbel, gumbel_ld   float32 [T][gumbel_ld] noise, as for tv_sample_tokens;
+ *                      may be NULL when every temperature is 0
+ *  uniforms            float32 [T], r_c ~ U(0, 1) for the edge into node c
+ *  cu_nodes, temperature, vocab
+ *                      as for tv_sample_tokens
+ *  parents             int32 [T] local parent lists (parent[0] = -1,
+ *                      0 <= parent[i] < i; TV_ST_BAD_ROOT / TV_ST_BAD_PARENT)
+ *  draft_tokens        int32 [T]
+ *  draft_logp          float32 [T] draft log-probability of each node's token
+ *  max_nodes, max_depth, accept_path, accept_len, bonus
+ *                      as for tv_greedy_accept (accept_path lists the
+ *                      accepted prefix of the chosen path)
+ *  status              in/out: requests with non-zero status are skipped;
+ *                      TV_ST_BAD_SIZE, _BAD_ROOT, _BAD_PARENT,
+ *                      _BAD_TEMPERATURE or _PATH_OVERFLOW are OR-ed in
+ *                      (outputs untouched)
+ * All arrays are device memory; nothing is allocated. Returns TV_OK, or
+ * TV_ERR_BAD_SIZE / TV_ERR_NULL_POINTER / TV_ERR_CUDA without launching.
+ */
+int tv_rejection_accept(const float* logits, int64_t logits_ld, const float* draft_logits,
+                        int64_t draft_ld, const float* gumbel, int64_t gumbel_ld,
+                        const float* uniforms, const int32_t* cu_nodes,
+                        const float* temperature, const int32_t* parents,
+                        const int32_t* draft_tokens, const float* draft_logp, int32_t batch,
+                        int32_t max_nodes, int32_t max_depth, int32_t vocab,
+                        int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
+                        int32_t* status, void* stream);
 
 /*
  * Nodes (root included) of the trees tv_ddtree_build makes: 1 + min(budget,

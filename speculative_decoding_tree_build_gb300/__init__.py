@@ -19,7 +19,7 @@ __all__ = [
     "TV_OK", "TV_ST", "TvGeom", "TvError", "load", "lib_path", "geom", "workspace_bytes",
     "tree_build", "tree_attention_verify", "tree_attention_verify_noalloc", "greedy_accept", "kv_commit",
     "accept_commit",
-    "sample_tokens", "sampled_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
+    "sample_tokens", "sampled_accept", "rejection_accept", "ddtree_nodes", "ddtree_topk", "ddtree_build",
     "eagle_expand_select", "eagle_rerank", "tree_mask_dense", "dense_mask_elements",
     "status_string", "version",
 ]
@@ -62,6 +62,8 @@ _SIGS = {
                      _P, _P, _P, _P],
     "tv_sample_tokens": [_P, _I64, _P, _I64, _P, _P, _I, _I, _I, _P, _P, _P],
     "tv_sampled_accept": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
+    "tv_rejection_accept": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                            _P, _P, _P, _P, _P],
     "tv_ddtree_nodes": [_I, _I, _I],
     "tv_ddtree_topk": [_P, _I64, _I, _I, _I, _P, _P, _P],
     "tv_ddtree_build": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P],
@@ -245,6 +247,25 @@ def sampled_accept(logits, gumbel, cu_nodes, temperature, parents, draft_tokens,
         _ptr(draft_tokens, I32, "draft_tokens"), batch, max_nodes, accept_path.shape[1] - 1,
         logits.shape[1], _ptr(accept_path, I32), _ptr(accept_len, I32), _ptr(bonus, I32),
         _ptr(status, I32), _stream(stream)))
+
+
+def rejection_accept(logits, draft_logits, gumbel, uniforms, cu_nodes, temperature, parents,
+                     draft_tokens, draft_logp, max_nodes, accept_path, accept_len, bonus, status,
+                     stream=None):
+    """Rejection-sampling verification along the chosen path (largest
+    cumulative draft log-probability): the min(1, p/q) rule per edge, the
+    correction drawn from the residual; same outputs as greedy_accept."""
+    batch = cu_nodes.numel() - 1
+    lp, lld = _rows(logits, "logits")
+    dp, dld = _rows(draft_logits, "draft_logits")
+    gp, gld = _rows(gumbel, "gumbel")
+    return _check("tv_rejection_accept", load().tv_rejection_accept(
+        lp, lld, dp, dld, gp, gld, _ptr(uniforms, torch.float32, "uniforms"),
+        _ptr(cu_nodes, I32, "cu_nodes"), _ptr(temperature, torch.float32, "temperature"),
+        _ptr(parents, I32, "parents"), _ptr(draft_tokens, I32, "draft_tokens"),
+        _ptr(draft_logp, torch.float32, "draft_logp"), batch, max_nodes,
+        accept_path.shape[1] - 1, logits.shape[1], _ptr(accept_path, I32), _ptr(accept_len, I32),
+        _ptr(bonus, I32), _ptr(status, I32), _stream(stream)))
 
 
 def ddtree_nodes(depth_L: int, k: int, budget: int) -> int:

@@ -310,6 +310,52 @@ def sampling_inputs(rng, w, vocab=None, sigma=1.0, boost=(8.0, 16.0), ld=None,
     return logits, gumbel
 
 
+def rejection_inputs(rng, w, vocab=None, draft_sigma=1.0, draft_boost=(4.0, 10.0), tau=0.5,
+                     ld=None, pad_value=np.nan):
+    """Inputs of the rejection-sampling walk: the drafter's logits at every
+    node, the target's, Gumbel noise, uniforms and draft log-probabilities.
+
+    draft[t] ~ N(0, draft_sigma) with every child's token raised by a boost
+    drawn from U(draft_boost) (the children are the drafter's likely tokens);
+    the target's row is the drafter's plus N(0, tau) noise (a drafter that
+    approximates the target); draft_logp[t] is the drafter's reported
+    log-probability of node t's token, drawn as -Exp(1) (the root's entry is
+    0 and unused); uniforms[t] ~ U(0, 1) in float32. Rows have ``ld`` >=
+    vocab columns, the ones past the vocabulary hold ``pad_value``. Returns
+    (logits, draft, gumbel, uniforms, draft_logp)."""
+    vocab = w["vocab"] if vocab is None else vocab
+    ld = vocab if ld is None else ld
+    cu = w["cu_nodes"]
+    total = int(cu[-1])
+    draft = np.empty((total, ld), np.float32)
+    logits = np.empty((total, ld), np.float32)
+    gumbel = np.empty((total, ld), np.float32)
+    noise = np.empty(vocab, np.float32)
+    for r in range(total):
+        rng.standard_normal(dtype=np.float32, out=draft[r, :vocab])
+        if draft_sigma != 1.0:
+            draft[r, :vocab] *= np.float32(draft_sigma)
+    for b in range(w["batch"]):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        par = w["parents"][t0:t1]
+        tok = w["draft_tokens"][t0:t1]
+        for j in range(1, t1 - t0):
+            if 0 <= int(tok[j]) < vocab:
+                draft[t0 + int(par[j]), int(tok[j])] += np.float32(rng.uniform(*draft_boost))
+    for r in range(total):
+        rng.standard_normal(dtype=np.float32, out=noise)
+        noise *= np.float32(tau)
+        np.add(draft[r, :vocab], noise, out=logits[r, :vocab])
+        _fill_gumbel(rng, gumbel[r, :vocab])
+    if ld > vocab:
+        for a in (draft, logits, gumbel):
+            a[:, vocab:] = pad_value
+    draft_logp = (-rng.standard_exponential(total)).astype(np.float32)
+    draft_logp[cu[:-1]] = 0.0
+    uniforms = rng.random(total, dtype=np.float32)
+    return logits, draft, gumbel, uniforms, draft_logp
+
+
 # --------------------------------------------------------------------------
 # batches
 

@@ -33,7 +33,7 @@ def header_functions():
 def test_header_declares_the_step_calls():
     names = header_functions()
     for want in ("tv_tree_build", "tv_tree_attention_verify", "tv_greedy_accept", "tv_kv_commit",
-                 "tv_sample_tokens", "tv_sampled_accept", "tv_ddtree_topk", "tv_ddtree_build",
+                 "tv_sample_tokens", "tv_sampled_accept", "tv_rejection_accept", "tv_ddtree_topk", "tv_ddtree_build",
                  "tv_ddtree_nodes", "tv_eagle_expand_select", "tv_eagle_rerank",
                  "tv_tree_mask_dense", "tv_accept_commit",
                  "tv_workspace_bytes",
@@ -119,6 +119,20 @@ def test_host_validation_rejects_before_launch(lib):
     assert A(*args[:10], -1, *args[11:]) == -3                          # max_depth
     assert A(*args[:6], None, *args[7:]) == -1                          # parents
     assert A(P + 4, *args[1:]) == -5
+    # rejection-sampling acceptance
+    Rj = L.tv_rejection_accept
+    args = [P, 32000, P, 32000, P, 32000, P, P, P, P, P, P, 1, 8, 4, 32000, P, P, P, P, None]
+    assert Rj(*args[:12], 0, *args[13:]) == 0                           # empty batch
+    assert Rj(*args[:13], 1025, *args[14:]) == -3                       # max_nodes
+    assert Rj(*args[:14], -1, *args[15:]) == -3                         # max_depth
+    assert Rj(*args[:15], 0, *args[16:]) == -3                          # vocab
+    assert Rj(P, 100, *args[2:]) == -3                                  # logits ld < vocab
+    assert Rj(*args[:3], 100, *args[4:]) == -3                          # draft ld < vocab
+    assert Rj(*args[:5], 100, *args[6:]) == -3                          # gumbel ld < vocab
+    assert Rj(*args[:4], None, 0, *args[6:12], 0, *args[13:]) == 0      # noise optional
+    assert Rj(*args[:2], None, *args[3:]) == -1                         # draft logits
+    assert Rj(*args[:11], None, *args[12:]) == -1                       # draft_logp
+    assert Rj(*args[:19], None, None) == -1                             # status
     # DDTree construction
     assert L.tv_ddtree_nodes(16, 256, 256) == 257
     assert L.tv_ddtree_nodes(3, 4, 6) == 7 and L.tv_ddtree_nodes(4, 2, 100) == 31
