@@ -96,7 +96,7 @@ def attn_source_sha():
     return source_sha(ATTN_SOURCES)
 
 
-SAMPLE_SOURCES = ("sample.cu", "tv_common.cuh")
+SAMPLE_SOURCES = ("sample.cu", "tv_cluster.cuh", "tv_common.cuh")
 
 
 DDTREE_SOURCES = ("ddtree.cu", "tv_common.cuh")
@@ -337,6 +337,70 @@ def measure_sampling(w, dev, stream, flush, iters, hbm_peak):
             "speedup_vs_sample_all_then_walk": us_sample / us_walk,
             "note": "latency-bound: one row per step per request, steps in sequence"},
     }
+
+
+def measure_rejection(w, dev, stream, flush, iters, hbm_peak):
+    """Rejection-sampling acceptance on the bench workload's trees: drafter
+    logits with boosted child tokens, target logits = drafter's + N(0, 0.5),
+    Gumbel noise, uniforms, draft log-probabilities (float32), temperature 1.
+    Times tv_rejection_accept with CUDA events, L2 flushed before each
+    launch. Algorithmic bytes: the target and drafter rows of every visited
+    node (the accepted prefix and the stop node) plus the stop node's noise
+    row; the kernel also reads the chosen path's rows past the stop node
+    (all path rows are reduced in parallel)."""
+    import torch
+
+    import speculative_decoding_tree_build_gb300 as tvb
+    from speculative_decoding_tree_build_gb300 import workloads as wl
+
+    rng = np.random.default_rng(5151 + int(w["config"]))
+    logits_h, draft_h, gumbel_h, unif_h, logp_h = wl.rejection_inputs(rng, w)
+    vocab = int(w["vocab"])
+    bsz = int(w["batch"])
+    logits, draft_l, gumbel = (torch.from_numpy(a).to(dev) for a in (logits_h, draft_h, gumbel_h))
+    unif, logp = torch.from_numpy(unif_h).to(dev), torch.from_numpy(logp_h).to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    cu = torch.from_numpy(np.asarray(w["cu_nodes"], np.int32)).to(dev)
+    parents = torch.from_numpy(np.asarray(w["parents"], np.int32)).to(dev)
+    tokens = torch.from_numpy(np.asarray(w["draft_tokens"], np.int32)).to(dev)
+    temps = torch.ones(bsz, dtype=torch.float32, device=dev)
+    status = torch.zeros(bsz, **i32)
+    md = int(w["max_depth"])
+    path = torch.empty((bsz, md + 1), **i32)
+    alen, bonus = torch.empty(bsz, **i32), torch.empty(bsz, **i32)
+    mn = int(w["max_nodes"])
+
+    def run():
+        tvb.rejection_accept(logits, draft_l, gumbel, unif, cu, temps, parents, tokens, logp, mn,
+                             path, alen, bonus, status, stream)
+
+    for _ in range(3):
+        flush.zero_()
+        run()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+    if int(status.abs().sum()) != 0:
+        raise RuntimeError("rejection walk produced status flags")
+    acc = alen.cpu().numpy()
+    visited = int((acc + 1).sum())
+    algo = visited * vocab * 8 + bsz * vocab * 4
+    gbs = algo / (us * 1e-6) / 1e9
+    return {
+        "vocab": vocab, "temperature": 1.0, "requests": bsz,
+        "mean_accepted": float(acc.mean()),
+        "inputs": "float32 drafter logits N(0,1) + boosted children, target = drafter + N(0,0.5), "
+                  "float32 Gumbel noise and uniforms",
+        "us_per_launch": us, "visited_rows": visited, "algorithmic_bytes": algo,
+        "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
+        "requests_per_s": bsz / (us * 1e-6)}
 
 
 def source_sha(files):
@@ -738,6 +802,8 @@ def run_ours(args):
     }
     if args.sampling_steps > 0:
         line["sampling"] = measure_sampling(w, dev, stream, flush, args.sampling_steps, hbm_peak)
+        line["rejection_acceptance"] = measure_rejection(w, dev, stream, flush,
+                                                         args.sampling_steps, hbm_peak)
         line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps,
                                                      hbm_peak)
         line["eagle_selection"] = measure_eagle(dev, stream, flush, args.sampling_steps)

@@ -339,16 +339,18 @@ int tv_sampled_accept(const float* logits, int64_t logits_ld, const float* gumbe
  *   p_u    softmax(logits[u] / T) (T == 0: all mass on the first argmax)
  *   q_u    softmax(draft_logits[u]), the distribution u's children were drawn from
  *   edge u -> c on the path is accepted when uniforms[c] < p_u(x_c) / q_u(x_c),
- *          x_c = draft_tokens[c] (q_u(x_c) == 0 accepts; x_c outside
- *          [0, vocab) rejects); the first rejection at u stops the walk
+ *          x_c = draft_tokens[c] (p_u(x_c) == 0 rejects, else
+ *          q_u(x_c) == 0 accepts; x_c outside [0, vocab) rejects); the first
+ *          rejection at u stops the walk
  *   bonus  after a rejection at u: Gumbel-max draw over max(0, p_u - q_u)
  *          (over p_u when that is zero everywhere) with noise row gumbel[u];
  *          after the whole path: draw over p at the last node; T == 0: the
  *          first argmax of the stop node's logits.
- * Log-sum-exps are reduced in float32 and finished in float64; the per-edge
- * ratios in float64; the residual keys log(p_v - q_v) + g_v in float32. A
- * decision can therefore differ from an exact evaluation only where the
- * exact margin is within float32 rounding.
+ * The path sums are float64 (exact choice); log-sum-exps, per-edge ratios
+ * and the residual keys log(p_v - q_v) + g_v are float32, so a sampled
+ * decision can differ from an exact evaluation only where the exact margin
+ * is within float32 rounding. Greedy requests read only the target rows and
+ * decide exactly.
  *
  *  logits, logits_ld   float32 [T][logits_ld] target logits, row per node
  *                      (logits_ld >= vocab)

@@ -14,13 +14,15 @@ sampler: argmax_v (log w_v + g_v) draws from w / sum(w).
 Readings where the pages leave a step open (listed in the design doc as well):
   * the path goes from the root to the leaf with the largest cumulative draft
     log-probability (sum of the draft log-probabilities of its tokens), the
-    smallest node index on ties;
+    smallest node index on ties, a NaN sum counting as -inf;
   * the target distribution at node u is p_u = softmax(h_u / T) (T == 0:
     all mass on the first argmax), the draft distribution q_u = softmax(d_u)
     over the drafter's logits at u (the distribution u's children were
     drawn from);
   * edge u -> c is accepted when r_c < p_u(x_c) / q_u(x_c) (r_c ~ U(0, 1), one
-    per node, given as input);
+    per node, given as input); a token the target gives no mass is never
+    accepted (0/0 counts as 0), one the drafter gives none but the target
+    some always is;
   * the correction after a rejection at u is drawn from the residual
     max(0, p_u - q_u) (the lossless choice of the speculative-sampling rule
     the page refers to; when the residual is zero everywhere, from p_u), with
@@ -43,7 +45,8 @@ def chosen_path_ref(parents, draft_logp):
         score[i] = score[parents[i]] + float(draft_logp[i])
         has_child[parents[i]] = True
     leaves = [i for i in range(n) if not has_child[i]]
-    best = max(leaves, key=lambda i: (score[i], -i))
+    key = np.where(np.isnan(score), -np.inf, score)
+    best = max(leaves, key=lambda i: (key[i], -i))
     path = [best]
     while path[-1] != 0:
         path.append(int(parents[path[-1]]))
@@ -88,7 +91,12 @@ def rejection_walk_ref(parents, draft_tokens, draft_logp, target_logits, draft_l
         p = _target_probs(target_logits[u], temperature)
         q = _softmax(draft_logits[u])
         x = int(draft_tokens[c])
-        ratio = p[x] / q[x] if q[x] > 0 else np.inf
+        if p[x] == 0:
+            ratio = 0.0
+        elif q[x] == 0:
+            ratio = np.inf
+        else:
+            ratio = p[x] / q[x]
         details["ratios"].append((float(uniforms[c]), float(ratio)))
         if float(uniforms[c]) < ratio:
             accepted.append(c)

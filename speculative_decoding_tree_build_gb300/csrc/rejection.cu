@@ -13,20 +13,25 @@
 //  1. every CTA stages the tree, sums each node's draft log-probabilities
 //     from the root (float64, one tree level per round) and walks up from the
 //     best leaf to get the path;
-//  2. for every path node each CTA reduces its slice of the target row (max,
-//     sum of exp(h / T), first argmax) and of the draft row (max, sum of
-//     exp(d)); one cluster barrier, then every CTA combines all slices'
-//     partials through distributed shared memory into the log-sum-exps;
-//  3. the per-edge decisions r < p(x) / q(x) are scalar work (the needed
-//     logits are gathered in parallel first), identical in every CTA;
-//  4. the stop node's rows are scanned once more for the Gumbel-max draw
-//     (residual first, p as the fallback), combined like step 2.
+//  2. the CTA's warps split the path rows of a pass (a row per warp at most) between
+//     them and reduce their segment of each row with 128-bit loads: sampling
+//     requests keep the online maximum and sum of exp(h / T) and of exp(d)
+//     (the log-sum-exps of p and q), greedy ones only the first argmax of h
+//     (p is one-hot, so q never matters and the drafter's rows are not read);
+//  3. one cluster barrier, then one warp per path row combines the cluster's
+//     partials (a lane per CTA, through distributed shared memory) and
+//     decides its edge, r < p(x) / q(x); a ballot finds the first rejection;
+//  4. sampling requests scan the stop node's rows once more for the
+//     Gumbel-max draw (residual first, p as the fallback).
 #include "tv_cluster.cuh"
 
 namespace tv {
 
-constexpr int kRejThreads = 1024;
-constexpr int kRejMaxPath = 64;          // path nodes reduced per pass (longer paths: several)
+constexpr int kRejThreads = 512;
+constexpr int kRejWarps = kRejThreads / 32;
+constexpr int kRejMaxPath = kRejWarps;   // path rows per pass: at least one warp per row
+constexpr float kRejLog2e = 1.4426950408889634f;
+static_assert(kRejWarps <= 32, "one lane per warp in the block-level maxima");
 
 struct RejParams {
   const float* target;                   // [T][target_ld]
@@ -44,10 +49,12 @@ struct RejParams {
   int32_t* status;
   long long target_ld, draft_ld, gumbel_ld;
   int max_nodes, max_depth, vocab, csize;
+  int vec;                               // bit 0/1/2: target/draft/noise rows 16-byte aligned
 };
 
-// Per path node and CTA slice: target (max, sum of exp(h*inv - max), argmax
-// key) and draft (max, sum of exp(d - max)).
+// One (row, slice) partial: target (max, sum of exp(h/T - max)), drafter
+// (max, sum of exp(d - max)), packed first-argmax key of h. 24 bytes, read
+// remotely as three 64-bit words.
 struct RejPart {
   float tm, ts, dm, ds;
   uint64_t amax;
@@ -56,35 +63,151 @@ struct RejPart {
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   const float nm = fmaxf(m, m2);
   if (nm == -INFINITY) return;
-  s = (m == -INFINITY ? 0.0f : s * fast_exp2((m - nm) * 1.4426950408889634f)) +
-      (m2 == -INFINITY ? 0.0f : s2 * fast_exp2((m2 - nm) * 1.4426950408889634f));
+  s = (m == -INFINITY ? 0.0f : s * fast_exp2((m - nm) * kRejLog2e)) +
+      (m2 == -INFINITY ? 0.0f : s2 * fast_exp2((m2 - nm) * kRejLog2e));
   m = nm;
 }
 
-__global__ void __launch_bounds__(kRejThreads, 1) rejection_accept_kernel(const __grid_constant__ RejParams p) {
+// Running maximum m and sum s of exp(x - m); -inf entries add nothing.
+__device__ __forceinline__ void online_add(float& m, float& s, float x) {
+  if (x > m) {
+    s = s * fast_exp2((m - x) * kRejLog2e) + 1.0f;
+    m = x;
+  } else if (x != -INFINITY) {
+    s += fast_exp2((x - m) * kRejLog2e);
+  }
+}
+
+__device__ __forceinline__ void part_identity(RejPart& r) {
+  r.tm = -INFINITY; r.ts = 0.0f; r.dm = -INFINITY; r.ds = 0.0f; r.amax = 0ull;
+}
+
+__device__ __forceinline__ void part_merge(RejPart& a, const RejPart& b) {
+  lse_merge(a.tm, a.ts, b.tm, b.ts);
+  lse_merge(a.dm, a.ds, b.dm, b.ds);
+  a.amax = b.amax > a.amax ? b.amax : a.amax;
+}
+
+__device__ __forceinline__ RejPart part_shfl_xor(const RejPart& a, int o) {
+  RejPart r;
+  r.tm = __shfl_xor_sync(0xffffffffu, a.tm, o);
+  r.ts = __shfl_xor_sync(0xffffffffu, a.ts, o);
+  r.dm = __shfl_xor_sync(0xffffffffu, a.dm, o);
+  r.ds = __shfl_xor_sync(0xffffffffu, a.ds, o);
+  r.amax = __shfl_xor_sync(0xffffffffu, a.amax, o);
+  return r;
+}
+
+__device__ __forceinline__ RejPart part_warp_merge(RejPart a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part_merge(a, part_shfl_xor(a, o));
+  return a;
+}
+
+// One element of a path row: greedy keeps the first argmax of h, sampling
+// the two running log-sum-exps.
+template <bool kSample>
+__device__ __forceinline__ void row_element(RejPart& r, ThreadBest& tb, float h, float d, int v,
+                                            float inv_t) {
+  if (kSample) {
+    online_add(r.tm, r.ts, __fmul_rn(h, inv_t));
+    online_add(r.dm, r.ds, d);
+  } else {
+    tb.offer(h, v);
+  }
+}
+
+// A warp's reduction of columns [a, b) of one target row (and drafter row
+// when sampling). a is a multiple of 4; with `vec` the rows are read as
+// float4, four loads in flight per lane and array.
+template <bool kSample>
+__device__ __forceinline__ RejPart reduce_segment(const float* hr, const float* dr, int a, int b,
+                                                  bool vec, float inv_t, int lane) {
+  RejPart r;
+  part_identity(r);
+  ThreadBest tb;
+  if (vec) {
+    const int b4 = a + ((b - a) & ~3);
+    for (int v = a + lane * 4; v < b4; v += 4 * 128) {
+      float4 h4[4], d4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int vj = v + j * 128;
+        if (vj < b4) {
+          h4[j] = __ldcs(reinterpret_cast<const float4*>(hr + vj));
+          if (kSample) d4[j] = __ldcs(reinterpret_cast<const float4*>(dr + vj));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int vj = v + j * 128;
+        if (vj < b4) {
+          row_element<kSample>(r, tb, h4[j].x, kSample ? d4[j].x : 0.0f, vj, inv_t);
+          row_element<kSample>(r, tb, h4[j].y, kSample ? d4[j].y : 0.0f, vj + 1, inv_t);
+          row_element<kSample>(r, tb, h4[j].z, kSample ? d4[j].z : 0.0f, vj + 2, inv_t);
+          row_element<kSample>(r, tb, h4[j].w, kSample ? d4[j].w : 0.0f, vj + 3, inv_t);
+        }
+      }
+    }
+    for (int v = b4 + lane; v < b; v += 32)
+      row_element<kSample>(r, tb, __ldcs(hr + v), kSample ? __ldcs(dr + v) : 0.0f, v, inv_t);
+  } else {
+#pragma unroll 4
+    for (int v = a + lane; v < b; v += 32)
+      row_element<kSample>(r, tb, __ldcs(hr + v), kSample ? __ldcs(dr + v) : 0.0f, v, inv_t);
+  }
+  r.amax = tb.packed();
+  return part_warp_merge(r);
+}
+
+}  // namespace tv
+
+namespace tv {
+
+// Draw keys of one element of the stop row: the residual's log(p - q) + g
+// (after a rejection) and p's fl(h / T) + g.
+__device__ __forceinline__ void draw_element(ThreadBest& res, ThreadBest& pb, float h, float d,
+                                             float g, int v, float inv_t, float lt, float ld,
+                                             bool rejected) {
+  const float x = __fmul_rn(h, inv_t);
+  pb.offer(__fadd_rn(x, g), v);
+  if (rejected) {
+    const float w = expf(x - lt) - expf(d - ld);
+    if (w > 0.0f) res.offer(__fadd_rn(logf(w), g), v);
+  }
+}
+
+__global__ void __launch_bounds__(kRejThreads, 1)
+    rejection_accept_kernel(const __grid_constant__ RejParams p) {
   __shared__ int s_par[TV_MAX_NODES];
+  __shared__ int s_tok[TV_MAX_NODES];
   __shared__ int s_path[TV_MAX_NODES];
+  __shared__ int s_depth[TV_MAX_NODES];
+  __shared__ float s_unif[TV_MAX_NODES];
   __shared__ double s_score[TV_MAX_NODES];
   __shared__ unsigned char s_leaf[TV_MAX_NODES];
-  __shared__ RejPart s_part[kRejMaxPath];          // this CTA's partials (read by the cluster)
-  __shared__ double s_lse_t[kRejMaxPath], s_lse_d[kRejMaxPath];
-  __shared__ int s_amax[kRejMaxPath];
-  __shared__ float s_wm[32], s_ws[32], s_wdm[32], s_wds[32];
-  __shared__ uint64_t s_wk[32], s_wk2[32];
-  __shared__ uint64_t s_draw[2];
-  __shared__ double s_hx[kRejMaxPath], s_dx[kRejMaxPath];
-  __shared__ int s_plen, s_best, s_stop, s_acc, s_rej;
+  __shared__ RejPart s_pw[kRejWarps];              // per-warp partials of this CTA
+  __shared__ RejPart s_part[kRejMaxPath];          // per-row partials of this CTA (read remotely)
+  __shared__ float s_hx[kRejMaxPath], s_dx[kRejMaxPath];
+  __shared__ float s_lt[kRejMaxPath], s_ld[kRejMaxPath];
+  __shared__ int s_am[kRejMaxPath], s_dec[kRejMaxPath];
+  __shared__ double s_bs[kRejWarps];
+  __shared__ int s_bi[kRejWarps];
+  __shared__ uint64_t s_wk[kRejWarps], s_wk2[kRejWarps], s_draw[2];
+  __shared__ int s_plen;
   grid_dependency_wait();
   grid_launch_dependents();
   const int b = blockIdx.y;
   const int csize = p.csize;
   const int rank = csize > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int st = p.status[b];
   const int t0 = p.cu_nodes[b];
   const int n = p.cu_nodes[b + 1] - t0;
   const float temp = p.temperature[b];
-  if (st != 0) return;                                   // uniform across the cluster
+  // every early exit below depends only on the request's inputs, so it is
+  // taken by all CTAs of the cluster alike
+  if (st != 0) return;
   if (n < 1 || n > p.max_nodes) {
     if (rank == 0 && threadIdx.x == 0) atomicOr(&p.status[b], TV_ST_BAD_SIZE);
     return;
@@ -94,12 +217,15 @@ __global__ void __launch_bounds__(kRejThreads, 1) rejection_accept_kernel(const 
     if (rank == 0 && threadIdx.x == 0) atomicOr(&p.status[b], tflag);
     return;
   }
-  // ---- 1. path: best cumulative draft log-probability, root to leaf
+  // ---- 1. the chosen path: largest cumulative draft log-probability
   int bad_root = 0, bad_par = 0;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int par = p.parents[t0 + i];
     s_par[i] = par;
+    s_tok[i] = p.draft_tokens[t0 + i];
+    s_unif[i] = p.uniforms[t0 + i];
     s_leaf[i] = 1;
+    s_depth[i] = i == 0 ? 1 : 0;
     s_score[i] = i == 0 ? 0.0 : static_cast<double>(p.draft_logp[t0 + i]);
     if (i == 0 && par != -1) bad_root = 1;
     if (i > 0 && (par < 0 || par >= i)) bad_par = 1;
@@ -112,51 +238,46 @@ __global__ void __launch_bounds__(kRejThreads, 1) rejection_accept_kernel(const 
     return;
   }
   for (int i = threadIdx.x + 1; i < n; i += blockDim.x) s_leaf[s_par[i]] = 0;
-  // scores: one tree level per round (a node adds its parent's finished score)
-  {
-    __shared__ int s_depth[TV_MAX_NODES];
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s_depth[i] = i == 0 ? 1 : 0;
-    __syncthreads();
-    for (int round = 1; round < n; ++round) {
-      int pending = 0;
-      for (int i = threadIdx.x + 1; i < n; i += blockDim.x) {
-        if (s_depth[i] != 0) continue;
-        if (s_depth[s_par[i]] == round) {
-          s_score[i] = s_score[s_par[i]] + s_score[i];
-          s_depth[i] = round + 1;
-        } else {
-          pending = 1;
-        }
+  // one tree level per round: a node adds its parent's finished score (the
+  // parent's level was set in an earlier round, so its score is final)
+  for (int round = 1; round < n; ++round) {
+    int pending = 0;
+    for (int i = threadIdx.x + 1; i < n; i += blockDim.x) {
+      if (s_depth[i] != 0) continue;
+      if (s_depth[s_par[i]] == round) {
+        s_score[i] = s_score[s_par[i]] + s_score[i];
+        s_depth[i] = round + 1;
+      } else {
+        pending = 1;
       }
-      if (!__syncthreads_or(pending)) break;
     }
+    if (!__syncthreads_or(pending)) break;
   }
   {
-    // best leaf: largest score, smallest index on ties
     double bs = -INFINITY;
     int bi = INT_MAX;
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-      if (s_leaf[i] && (s_score[i] > bs || (s_score[i] == bs && i < bi))) { bs = s_score[i]; bi = i; }
+    // a NaN score counts as -inf, so some leaf is always chosen
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const double sc = s_score[i] != s_score[i] ? -INFINITY : s_score[i];
+      if (s_leaf[i] && (sc > bs || (sc == bs && i < bi))) { bs = sc; bi = i; }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const double os = __shfl_xor_sync(0xffffffffu, bs, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (os > bs || (os == bs && oi < bi)) { bs = os; bi = oi; }
     }
-    __shared__ double s_bs[32];
-    __shared__ int s_bi[32];
     if (lane == 0) { s_bs[warp] = bs; s_bi[warp] = bi; }
     __syncthreads();
     if (threadIdx.x == 0) {
       double cs = s_bs[0];
       int ci = s_bi[0];
-      for (int w = 1; w < nw; ++w)
+      for (int w = 1; w < kRejWarps; ++w)
         if (s_bs[w] > cs || (s_bs[w] == cs && s_bi[w] < ci)) { cs = s_bs[w]; ci = s_bi[w]; }
-      // walk up, then reverse into root-first order
-      int len = 0, u = ci;
-      while (u >= 0 && len < TV_MAX_NODES) { s_path[len++] = u; u = s_par[u]; }
-      for (int a = 0, z = len - 1; a < z; ++a, --z) { const int t = s_path[a]; s_path[a] = s_path[z]; s_path[z] = t; }
+      // the depth of the leaf is its path length; fill root-first
+      int u = ci, len = s_depth[ci];
       s_plen = len;
+      for (int k = len - 1; k >= 0 && u >= 0; --k) { s_path[k] = u; u = s_par[u]; }
     }
     __syncthreads();
   }
@@ -165,168 +286,157 @@ __global__ void __launch_bounds__(kRejThreads, 1) rejection_accept_kernel(const 
   slice_of(p.vocab, rank, csize, v0, v1);
   const bool sample = temp > 0.0f;
   const float inv_t = sample ? __frcp_rn(temp) : 1.0f;
-  const float kL2e = 1.4426950408889634f;
-  // ---- 2./3. log-sum-exps of the path rows, then the decisions, in passes
-  // of kRejMaxPath path nodes (a pass ends where a rejection happened)
-  int acc = 0;                     // accepted edges so far
-  int stop = -1;                   // path index of the node the draw happens at
+  const bool vec_t = p.vec & 1, vec_d = (p.vec & 2) != 0, vec_g = (p.vec & 4) != 0;
+  // ---- 2./3. passes of up to kRejMaxPath path rows
+  int acc = 0;                 // accepted edges
+  int stop = -1;               // path index of the node the draw happens at
   bool rejected = false;
-  for (int base = 0; base < plen && stop < 0; base += kRejMaxPath) {
+  for (int base = 0; stop < 0; base += kRejMaxPath) {
     const int cnt = min(kRejMaxPath, plen - base);
-    for (int k = 0; k < cnt; ++k) {
+    // the logits of each edge's token (sampling), fetched while the rows stream
+    if (sample && threadIdx.x < cnt && base + threadIdx.x + 1 < plen) {
+      const int k = threadIdx.x;
       const size_t u = static_cast<size_t>(t0 + s_path[base + k]);
+      const int x = s_tok[s_path[base + k + 1]];
+      const bool inside = x >= 0 && x < p.vocab;
+      s_hx[k] = inside ? p.target[u * p.target_ld + x] : -INFINITY;
+      s_dx[k] = inside ? p.draft[u * p.draft_ld + x] : -INFINITY;
+    }
+    // warps split over the rows: wpr warps per row, each a segment of the slice
+    const int wpr = kRejWarps / cnt;
+    const int k = warp / wpr, seg = warp % wpr;
+    if (k < cnt) {
+      const size_t u = static_cast<size_t>(t0 + s_path[base + k]);
+      const int seglen = (((v1 - v0) + wpr - 1) / wpr + 3) & ~3;
+      const int a = min(v1, v0 + seg * seglen), e = min(v1, a + seglen);
       const float* hr = p.target + u * p.target_ld;
       const float* dr = p.draft + u * p.draft_ld;
-      float tm = -INFINITY, ts = 0.0f, dm = -INFINITY, ds = 0.0f;
-      ThreadBest tb;
-      for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-        const float h = __ldcs(hr + v);
-        tb.offer(h, v);
-        const float x = sample ? __fmul_rn(h, inv_t) : h;
-        lse_merge(tm, ts, x, 1.0f);
-        lse_merge(dm, ds, __ldcs(dr + v), 1.0f);
-      }
-      uint64_t key = tb.packed();
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lse_merge(tm, ts, __shfl_xor_sync(0xffffffffu, tm, o), __shfl_xor_sync(0xffffffffu, ts, o));
-        lse_merge(dm, ds, __shfl_xor_sync(0xffffffffu, dm, o), __shfl_xor_sync(0xffffffffu, ds, o));
-        const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, o);
-        key = ok > key ? ok : key;
-      }
-      if (lane == 0) { s_wm[warp] = tm; s_ws[warp] = ts; s_wdm[warp] = dm; s_wds[warp] = ds; s_wk[warp] = key; }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        RejPart r = {s_wm[0], s_ws[0], s_wdm[0], s_wds[0], s_wk[0]};
-        for (int w = 1; w < nw; ++w) {
-          lse_merge(r.tm, r.ts, s_wm[w], s_ws[w]);
-          lse_merge(r.dm, r.ds, s_wdm[w], s_wds[w]);
-          r.amax = s_wk[w] > r.amax ? s_wk[w] : r.amax;
-        }
-        s_part[k] = r;
-      }
-      __syncthreads();
+      const RejPart r = sample ? reduce_segment<true>(hr, dr, a, e, vec_t && vec_d, inv_t, lane)
+                               : reduce_segment<false>(hr, dr, a, e, vec_t, inv_t, lane);
+      if (lane == 0) s_pw[warp] = r;
+    }
+    __syncthreads();
+    if (warp < cnt) {
+      RejPart r;
+      part_identity(r);
+      if (lane < wpr) r = s_pw[warp * wpr + lane];
+      r = part_warp_merge(r);
+      if (lane == 0) s_part[warp] = r;
     }
     row_barrier(csize);
-    // combine the cluster's partials (each CTA for itself)
-    if (threadIdx.x < cnt) {
-      const int k = threadIdx.x;
-      float tm = -INFINITY, ts = 0.0f, dm = -INFINITY, ds = 0.0f;
-      uint64_t am = 0ull;
-      for (int r = 0; r < csize; ++r) {
-        RejPart q;
+    // one warp per row: combine the cluster's partials, decide the edge
+    if (warp < cnt) {
+      RejPart r;
+      part_identity(r);
+      if (lane < csize) {
         if (csize > 1) {
-          const uint64_t* src = reinterpret_cast<const uint64_t*>(&s_part[k]);
-          uint64_t w0 = ld_cluster_u64(src, r), w1 = ld_cluster_u64(src + 1, r), w2 = ld_cluster_u64(src + 2, r);
-          q.tm = __uint_as_float(static_cast<uint32_t>(w0));
-          q.ts = __uint_as_float(static_cast<uint32_t>(w0 >> 32));
-          q.dm = __uint_as_float(static_cast<uint32_t>(w1));
-          q.ds = __uint_as_float(static_cast<uint32_t>(w1 >> 32));
-          q.amax = w2;
+          const uint64_t* src = reinterpret_cast<const uint64_t*>(&s_part[warp]);
+          const uint64_t w0 = ld_cluster_u64(src, lane), w1 = ld_cluster_u64(src + 1, lane);
+          const uint64_t w2 = ld_cluster_u64(src + 2, lane);
+          r.tm = __uint_as_float(static_cast<uint32_t>(w0));
+          r.ts = __uint_as_float(static_cast<uint32_t>(w0 >> 32));
+          r.dm = __uint_as_float(static_cast<uint32_t>(w1));
+          r.ds = __uint_as_float(static_cast<uint32_t>(w1 >> 32));
+          r.amax = w2;
         } else {
-          q = s_part[k];
+          r = s_part[warp];
         }
-        lse_merge(tm, ts, q.tm, q.ts);
-        lse_merge(dm, ds, q.dm, q.ds);
-        am = q.amax > am ? q.amax : am;
       }
-      s_lse_t[k] = static_cast<double>(tm) + log(static_cast<double>(ts));
-      s_lse_d[k] = static_cast<double>(dm) + log(static_cast<double>(ds));
-      s_amax[k] = best_index(am);
-    }
-    // the logits of each edge's token, gathered in parallel
-    if (threadIdx.x < cnt && base + threadIdx.x + 1 < plen) {
-      const int k = threadIdx.x;
-      const size_t u = static_cast<size_t>(t0 + s_path[base + k]);
-      const int x = p.draft_tokens[t0 + s_path[base + k + 1]];
-      const bool inside = x >= 0 && x < p.vocab;
-      s_hx[k] = inside ? static_cast<double>(p.target[u * p.target_ld + x]) : -INFINITY;
-      s_dx[k] = inside ? static_cast<double>(p.draft[u * p.draft_ld + x]) : -INFINITY;
+      r = part_warp_merge(r);
+      if (lane == 0) {
+        const int pi = base + warp;
+        const float lt = r.tm + logf(r.ts), ld = r.dm + logf(r.ds);
+        const int am = best_index(r.amax);
+        int dec = 0;                                 // 0: the walk stops at this node
+        if (pi + 1 < plen) {
+          const int c = s_path[pi + 1];
+          const int x = s_tok[c];
+          if (x < 0 || x >= p.vocab) {
+            dec = 0;                                 // outside the vocabulary: rejected
+          } else if (!sample) {
+            dec = x == am;                           // p is one-hot on the first argmax
+          } else {
+            const float hx = s_hx[warp], dx = s_dx[warp];
+            if (hx == -INFINITY) {
+              dec = 0;                               // p(x) = 0
+            } else if (dx == -INFINITY) {
+              dec = 1;                               // q(x) = 0 < p(x)
+            } else {
+              const float ratio = expf((__fmul_rn(hx, inv_t) - lt) - (dx - ld));
+              dec = s_unif[c] < ratio;
+            }
+          }
+        }
+        s_dec[warp] = dec;
+        s_lt[warp] = lt;
+        s_ld[warp] = ld;
+        s_am[warp] = am;
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int a = acc, s_at = -1;
-      bool rej = false;
-      for (int k = 0; k < cnt; ++k) {
-        const int pi = base + k;
-        if (pi + 1 >= plen) { s_at = pi; break; }         // the last node: bonus draw
-        const int x = p.draft_tokens[t0 + s_path[pi + 1]];
-        double pt;
-        if (sample) pt = exp(static_cast<double>(__fmul_rn(static_cast<float>(s_hx[k]), inv_t)) - s_lse_t[k]);
-        else pt = (x == s_amax[k]) ? 1.0 : 0.0;
-        const double qd = exp(s_dx[k] - s_lse_d[k]);
-        // a token outside the vocabulary is rejected
-        const double ratio = (x < 0 || x >= p.vocab) ? 0.0 : (qd > 0.0 ? pt / qd : INFINITY);
-        const double r = static_cast<double>(p.uniforms[t0 + s_path[pi + 1]]);
-        if (r < ratio) { ++a; continue; }
-        s_at = pi;
-        rej = true;
-        break;
-      }
-      s_acc = a;
-      s_stop = s_at;
-      s_rej = rej;
+    // the first row whose edge is not accepted (every warp finds it itself)
+    const unsigned stops = __ballot_sync(0xffffffffu, lane < cnt && s_dec[lane] == 0);
+    if (stops != 0u) {
+      const int ks = __ffs(stops) - 1;
+      acc += ks;
+      stop = base + ks;
+      rejected = stop + 1 < plen;
+    } else {
+      acc += cnt;
+      row_barrier(csize);                  // partials read everywhere before they are rewritten
     }
-    __syncthreads();
-    acc = s_acc;
-    stop = s_stop;
-    rejected = s_rej;
-    if (stop >= 0) {
-      // keep the stop node's log-sum-exps for the draw
-      if (threadIdx.x == 0) {
-        const int k = stop - base;
-        s_lse_t[0] = s_lse_t[k];
-        s_lse_d[0] = s_lse_d[k];
-        s_amax[0] = s_amax[k];
-      }
-      __syncthreads();
-    }
-    row_barrier(csize);                        // partials read before the next pass rewrites them
   }
   // ---- 4. the draw at the stop node
-  const size_t su = static_cast<size_t>(t0 + s_path[stop]);
-  int tok;
-  if (!sample) {
-    // all of p on the first argmax: the residual's mass, and p's, sits there
-    tok = s_amax[0];
-  } else {
+  const int ks = stop % kRejMaxPath;
+  int tok = s_am[ks];                      // greedy: all of p, and of the residual, is there
+  if (sample) {
+    const size_t su = static_cast<size_t>(t0 + s_path[stop]);
     const float* hr = p.target + su * p.target_ld;
     const float* dr = p.draft + su * p.draft_ld;
     const float* gr = p.gumbel + su * p.gumbel_ld;
-    const float lt = static_cast<float>(s_lse_t[0]), ld = static_cast<float>(s_lse_d[0]);
+    const float lt = s_lt[ks], ld = s_ld[ks];
     ThreadBest res, pb;
-    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-      const float x = __fmul_rn(__ldcs(hr + v), inv_t);
-      const float g = __ldcs(gr + v);
-      pb.offer(__fadd_rn(x, g), v);                      // log p_v + g_v up to a constant
-      if (rejected) {
-        const float pv = expf(x - lt), qv = expf(__ldcs(dr + v) - ld);
-        const float w = pv - qv;
-        if (w > 0.0f) res.offer(__fadd_rn(logf(w), g), v);
+    if (vec_t && vec_g && (vec_d || !rejected)) {
+      const int b4 = v0 + ((v1 - v0) & ~3);
+      for (int v = v0 + threadIdx.x * 4; v < b4; v += 4 * kRejThreads) {
+        const float4 h4 = __ldcs(reinterpret_cast<const float4*>(hr + v));
+        const float4 g4 = __ldcs(reinterpret_cast<const float4*>(gr + v));
+        const float4 d4 = rejected ? __ldcs(reinterpret_cast<const float4*>(dr + v))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        draw_element(res, pb, h4.x, d4.x, g4.x, v, inv_t, lt, ld, rejected);
+        draw_element(res, pb, h4.y, d4.y, g4.y, v + 1, inv_t, lt, ld, rejected);
+        draw_element(res, pb, h4.z, d4.z, g4.z, v + 2, inv_t, lt, ld, rejected);
+        draw_element(res, pb, h4.w, d4.w, g4.w, v + 3, inv_t, lt, ld, rejected);
       }
+      for (int v = b4 + threadIdx.x; v < v1; v += kRejThreads)
+        draw_element(res, pb, __ldcs(hr + v), rejected ? __ldcs(dr + v) : 0.0f, __ldcs(gr + v), v,
+                     inv_t, lt, ld, rejected);
+    } else {
+      for (int v = v0 + threadIdx.x; v < v1; v += kRejThreads)
+        draw_element(res, pb, __ldcs(hr + v), rejected ? __ldcs(dr + v) : 0.0f, __ldcs(gr + v), v,
+                     inv_t, lt, ld, rejected);
     }
-    uint64_t k1 = res.packed(), k2 = pb.packed();
-    k1 = warp_max_u64(k1);
-    k2 = warp_max_u64(k2);
+    const uint64_t k1 = warp_max_u64(res.packed()), k2 = warp_max_u64(pb.packed());
     if (lane == 0) { s_wk[warp] = k1; s_wk2[warp] = k2; }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint64_t a1 = 0ull, a2 = 0ull;
-      for (int w = 0; w < nw; ++w) { a1 = s_wk[w] > a1 ? s_wk[w] : a1; a2 = s_wk2[w] > a2 ? s_wk2[w] : a2; }
-      s_draw[0] = a1;
-      s_draw[1] = a2;
+    if (warp == 0) {
+      const uint64_t a1 = warp_max_u64(lane < kRejWarps ? s_wk[lane] : 0ull);
+      const uint64_t a2 = warp_max_u64(lane < kRejWarps ? s_wk2[lane] : 0ull);
+      if (lane == 0) { s_draw[0] = a1; s_draw[1] = a2; }
     }
     row_barrier(csize);
-    uint64_t a1 = 0ull, a2 = 0ull;
-    for (int r = 0; r < csize; ++r) {
-      const uint64_t x1 = csize > 1 ? ld_cluster_u64(&s_draw[0], r) : s_draw[0];
-      const uint64_t x2 = csize > 1 ? ld_cluster_u64(&s_draw[1], r) : s_draw[1];
-      a1 = x1 > a1 ? x1 : a1;
-      a2 = x2 > a2 ? x2 : a2;
+    if (rank == 0 && warp == 0) {
+      uint64_t x1 = 0ull, x2 = 0ull;
+      if (lane < csize) {
+        x1 = csize > 1 ? ld_cluster_u64(&s_draw[0], lane) : s_draw[0];
+        x2 = csize > 1 ? ld_cluster_u64(&s_draw[1], lane) : s_draw[1];
+      }
+      x1 = warp_max_u64(x1);
+      x2 = warp_max_u64(x2);
+      tok = (rejected && x1 != 0ull) ? best_index(x1) : best_index(x2);
     }
-    tok = (rejected && a1 != 0ull) ? best_index(a1) : best_index(a2);
   }
-  if (csize > 1) cluster_sync_all();             // remote reads done before any CTA exits
+  if (csize > 1) cluster_sync_all();        // remote reads done before any CTA exits
   if (rank != 0) return;
   if (acc > p.max_depth) {
     if (threadIdx.x == 0) atomicOr(&p.status[b], TV_ST_PATH_OVERFLOW);
@@ -362,8 +472,12 @@ extern "C" int tv_rejection_accept(const float* target_logits, int64_t target_ld
   const int dev = tv::current_device();
   const int sms = dev < 0 ? -1 : tv::device_sm_count(dev);
   if (sms <= 0) return TV_ERR_CUDA;
+  // one CTA per vocabulary slice; clusters while a CTA per SM stays for every slice
   int csize = 1;
-  while (csize < 8 && batch * csize * 2 * 2 <= sms) csize *= 2;
+  while (csize < 8 && batch * csize * 2 <= sms) csize *= 2;
+  auto rows16 = [](const void* ptr, int64_t ld) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0 && ld % 4 == 0;
+  };
   tv::RejParams p;
   p.target = target_logits;
   p.draft = draft_logits;
@@ -385,6 +499,8 @@ extern "C" int tv_rejection_accept(const float* target_logits, int64_t target_ld
   p.max_depth = max_depth;
   p.vocab = vocab;
   p.csize = csize;
+  p.vec = (rows16(target_logits, target_ld) ? 1 : 0) | (rows16(draft_logits, draft_ld) ? 2 : 0) |
+          (rows16(gumbel, gumbel_ld) ? 4 : 0);
   const cudaError_t err = tv::launch_cluster_pdl(tv::rejection_accept_kernel, dim3(csize, batch),
                                                  dim3(tv::kRejThreads), csize,
                                                  tv::as_stream(stream), p);

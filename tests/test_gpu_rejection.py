@@ -265,3 +265,27 @@ def test_ddtree_vocab():
     out = _run(w, inputs, temps, vocab)
     _, ties = _check(w, inputs, temps, vocab, out)
     assert ties <= 1
+
+
+def test_zero_mass_tokens_and_infinite_logits():
+    """-inf logits: a token the target rules out is rejected, one only the
+    drafter rules out is accepted; the residual draw skips -inf entries."""
+    vocab = 3
+    w = {"batch": 3, "max_nodes": 2, "max_depth": 1, "vocab": vocab,
+         "cu_nodes": np.array([0, 2, 4, 6], np.int32),
+         "parents": np.array([-1, 0, -1, 0, -1, 0], np.int32),
+         "draft_tokens": np.array([0, 2, 0, 1, 0, 1], np.int32)}
+    tl = np.array([[1.0, 0.5, -np.inf], [0.0, 0.0, 0.0]] * 3, np.float32)
+    dl = np.array([[0.0, -np.inf, -np.inf], [0.0, 0.0, 0.0]] * 3, np.float32)
+    g = np.zeros((6, vocab), np.float32)
+    g[1] = [0.0, 2.0, 0.0]
+    g[3] = [3.0, 0.0, 0.0]
+    unif = np.array([0.5, 0.5, 0.5, 0.999, 0.5, 0.0], np.float32)
+    logp = np.array([0, -1, 0, -1, 0, -1], np.float32)
+    inputs = (tl, dl, g, unif, logp)
+    temps = [1.0, 1.0, 0.0]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        out = _run(w, inputs, temps, vocab)
+        depths, ties = _check(w, inputs, temps, vocab, out)
+    path, alen, bonus, st = out
+    assert ties == 0 and list(alen) == [0, 1, 0] and list(bonus) == [1, 0, 0]

@@ -80,3 +80,23 @@ def test_chosen_path_by_cumulative_draft_logprob():
     logp = [0.0, -0.1, -0.5, -2.0, -1.0, -0.6]
     assert chosen_path_ref(parents, logp) == [0, 1, 4]     # tie -1.1: smaller index 4
     assert chosen_path_ref([-1], [0.0]) == [0]
+
+
+def test_zero_mass_tokens():
+    """A token the target gives no mass is rejected even when the drafter
+    gives it none either (0/0 counts as 0); a token only the drafter rules
+    out is accepted whatever the uniform."""
+    g = np.zeros((2, 3))
+    tl = np.array([[1.0, 0.5, -np.inf], [0.0, 0.0, 0.0]])
+    dl = np.array([[0.0, -np.inf, -np.inf], [0.0, 0.0, 0.0]])
+    st, acc, bonus, det = rejection_walk_ref([-1, 0], [0, 2], [0, -1], tl, dl, [0.5, 0.0], g,
+                                             1.0, 4)
+    assert st == 0 and acc == [0] and det["ratios"][0][1] == 0.0
+    assert bonus == 1                      # residual max(0, p - q) has mass on token 1 only
+    st, acc, bonus, det = rejection_walk_ref([-1, 0], [0, 1], [0, -1], tl, dl, [0.5, 0.999],
+                                             g, 1.0, 4)
+    assert st == 0 and acc == [0, 1] and det["ratios"][0][1] == np.inf
+    # greedy: a token other than the argmax is rejected even with q(x) = 0
+    st, acc, bonus, _ = rejection_walk_ref([-1, 0], [0, 1], [0, -1], tl, dl, [0.5, 0.0], g,
+                                           0.0, 4)
+    assert acc == [0] and bonus == 0
