@@ -11,8 +11,8 @@
 //
 // One cluster per request (a CTA per vocabulary slice):
 //  1. every CTA stages the tree, sums each node's draft log-probabilities
-//     from the root (float64, one tree level per round) and walks up from the
-//     best leaf to get the path;
+//     from the root (float64, one tree level per round), picks the best leaf
+//     by integer keys of those sums and walks up from it to get the path;
 //  2. the CTA's warps split the path rows of a pass (a row per warp at most) between
 //     them and reduce their segment of each row with 128-bit loads: sampling
 //     requests keep the online maximum and sum of exp(h / T) and of exp(d)
@@ -30,6 +30,7 @@ namespace tv {
 constexpr int kRejThreads = 512;
 constexpr int kRejWarps = kRejThreads / 32;
 constexpr int kRejMaxPath = kRejWarps;   // path rows per pass: at least one warp per row
+constexpr int kRejUnroll = 4;            // float4 loads in flight per lane and row array
 constexpr float kRejLog2e = 1.4426950408889634f;
 static_assert(kRejWarps <= 32, "one lane per warp in the block-level maxima");
 
@@ -78,6 +79,41 @@ __device__ __forceinline__ void online_add(float& m, float& s, float x) {
   }
 }
 
+// Four entries at once: one rescale at most. exp2 of -inf is 0, so -inf
+// entries (and the empty start, m = -inf, s = 0) need no test.
+__device__ __forceinline__ void online_add4(float& m, float& s, float a, float b, float c,
+                                            float d) {
+  const float mx = fmaxf(fmaxf(a, b), fmaxf(c, d));
+  if (mx == -INFINITY) return;
+  if (mx > m) {
+    s *= fast_exp2((m - mx) * kRejLog2e);
+    m = mx;
+  }
+  s += (fast_exp2((a - m) * kRejLog2e) + fast_exp2((b - m) * kRejLog2e)) +
+       (fast_exp2((c - m) * kRejLog2e) + fast_exp2((d - m) * kRejLog2e));
+}
+
+// Total order on float64 path sums as unsigned keys (NaN as -inf, -0 as +0),
+// so the best leaf is found with integer reductions (float64 is slow here);
+// every key is above 0, the key of "no leaf".
+__device__ __forceinline__ uint64_t score_key(double x) {
+  uint64_t u = static_cast<uint64_t>(__double_as_longlong(x));
+  const uint64_t mag = u & 0x7FFFFFFFFFFFFFFFull;
+  if (mag > 0x7FF0000000000000ull) u = 0xFFF0000000000000ull;   // NaN -> -inf
+  if (mag == 0) u = 0;                                           // -0 -> +0
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// Warp-wide (largest key, smallest index among it); lanes without a
+// candidate hold (0, INT_MAX).
+__device__ __forceinline__ void warp_best_leaf(uint64_t& key, int& idx) {
+  const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
+  const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+  idx = __reduce_min_sync(0xffffffffu, (hi == mhi && lo == mlo) ? idx : INT_MAX);
+  key = (static_cast<uint64_t>(mhi) << 32) | mlo;
+}
+
 __device__ __forceinline__ void part_identity(RejPart& r) {
   r.tm = -INFINITY; r.ts = 0.0f; r.dm = -INFINITY; r.ds = 0.0f; r.amax = 0ull;
 }
@@ -119,7 +155,7 @@ __device__ __forceinline__ void row_element(RejPart& r, ThreadBest& tb, float h,
 
 // A warp's reduction of columns [a, b) of one target row (and drafter row
 // when sampling). a is a multiple of 4; with `vec` the rows are read as
-// float4, four loads in flight per lane and array.
+// float4, kRejUnroll loads in flight per lane and array.
 template <bool kSample>
 __device__ __forceinline__ RejPart reduce_segment(const float* hr, const float* dr, int a, int b,
                                                   bool vec, float inv_t, int lane) {
@@ -128,10 +164,10 @@ __device__ __forceinline__ RejPart reduce_segment(const float* hr, const float* 
   ThreadBest tb;
   if (vec) {
     const int b4 = a + ((b - a) & ~3);
-    for (int v = a + lane * 4; v < b4; v += 4 * 128) {
-      float4 h4[4], d4[4];
+    for (int v = a + lane * 4; v < b4; v += kRejUnroll * 128) {
+      float4 h4[kRejUnroll], d4[kRejUnroll];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kRejUnroll; ++j) {
         const int vj = v + j * 128;
         if (vj < b4) {
           h4[j] = __ldcs(reinterpret_cast<const float4*>(hr + vj));
@@ -139,13 +175,19 @@ __device__ __forceinline__ RejPart reduce_segment(const float* hr, const float* 
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kRejUnroll; ++j) {
         const int vj = v + j * 128;
         if (vj < b4) {
-          row_element<kSample>(r, tb, h4[j].x, kSample ? d4[j].x : 0.0f, vj, inv_t);
-          row_element<kSample>(r, tb, h4[j].y, kSample ? d4[j].y : 0.0f, vj + 1, inv_t);
-          row_element<kSample>(r, tb, h4[j].z, kSample ? d4[j].z : 0.0f, vj + 2, inv_t);
-          row_element<kSample>(r, tb, h4[j].w, kSample ? d4[j].w : 0.0f, vj + 3, inv_t);
+          if (kSample) {
+            online_add4(r.tm, r.ts, __fmul_rn(h4[j].x, inv_t), __fmul_rn(h4[j].y, inv_t),
+                        __fmul_rn(h4[j].z, inv_t), __fmul_rn(h4[j].w, inv_t));
+            online_add4(r.dm, r.ds, d4[j].x, d4[j].y, d4[j].z, d4[j].w);
+          } else {
+            tb.offer(h4[j].x, vj);
+            tb.offer(h4[j].y, vj + 1);
+            tb.offer(h4[j].z, vj + 2);
+            tb.offer(h4[j].w, vj + 3);
+          }
         }
       }
     }
@@ -191,7 +233,7 @@ __global__ void __launch_bounds__(kRejThreads, 1)
   __shared__ float s_hx[kRejMaxPath], s_dx[kRejMaxPath];
   __shared__ float s_lt[kRejMaxPath], s_ld[kRejMaxPath];
   __shared__ int s_am[kRejMaxPath], s_dec[kRejMaxPath];
-  __shared__ double s_bs[kRejWarps];
+  __shared__ uint64_t s_bk[kRejWarps];
   __shared__ int s_bi[kRejWarps];
   __shared__ uint64_t s_wk[kRejWarps], s_wk2[kRejWarps], s_draw[2];
   __shared__ int s_plen;
@@ -254,30 +296,28 @@ __global__ void __launch_bounds__(kRejThreads, 1)
     if (!__syncthreads_or(pending)) break;
   }
   {
-    double bs = -INFINITY;
+    // the best leaf by integer keys (a NaN score counts as -inf)
+    uint64_t bk = 0ull;
     int bi = INT_MAX;
-    // a NaN score counts as -inf, so some leaf is always chosen
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const double sc = s_score[i] != s_score[i] ? -INFINITY : s_score[i];
-      if (s_leaf[i] && (sc > bs || (sc == bs && i < bi))) { bs = sc; bi = i; }
+      if (!s_leaf[i]) continue;
+      const uint64_t k = score_key(s_score[i]);
+      if (k > bk) { bk = k; bi = i; }        // a thread's indices increase: ties keep the first
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double os = __shfl_xor_sync(0xffffffffu, bs, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (os > bs || (os == bs && oi < bi)) { bs = os; bi = oi; }
-    }
-    if (lane == 0) { s_bs[warp] = bs; s_bi[warp] = bi; }
+    warp_best_leaf(bk, bi);
+    if (lane == 0) { s_bk[warp] = bk; s_bi[warp] = bi; }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double cs = s_bs[0];
-      int ci = s_bi[0];
-      for (int w = 1; w < kRejWarps; ++w)
-        if (s_bs[w] > cs || (s_bs[w] == cs && s_bi[w] < ci)) { cs = s_bs[w]; ci = s_bi[w]; }
-      // the depth of the leaf is its path length; fill root-first
-      int u = ci, len = s_depth[ci];
-      s_plen = len;
-      for (int k = len - 1; k >= 0 && u >= 0; --k) { s_path[k] = u; u = s_par[u]; }
+    if (warp == 0) {
+      bk = lane < kRejWarps ? s_bk[lane] : 0ull;
+      bi = lane < kRejWarps ? s_bi[lane] : INT_MAX;
+      warp_best_leaf(bk, bi);
+      if (lane == 0) {
+        // the leaf's level is its path length; fill root-first
+        int u = bi;
+        const int len = s_depth[bi];
+        s_plen = len;
+        for (int k = len - 1; k >= 0 && u >= 0; --k) { s_path[k] = u; u = s_par[u]; }
+      }
     }
     __syncthreads();
   }
@@ -473,6 +513,8 @@ extern "C" int tv_rejection_accept(const float* target_logits, int64_t target_ld
   const int sms = dev < 0 ? -1 : tv::device_sm_count(dev);
   if (sms <= 0) return TV_ERR_CUDA;
   // one CTA per vocabulary slice; clusters while a CTA per SM stays for every slice
+  // one CTA (one SM) per vocabulary slice: the widest portable power-of-two
+  // cluster that keeps the whole batch within half the SMs
   int csize = 1;
   while (csize < 8 && batch * csize * 2 <= sms) csize *= 2;
   auto rows16 = [](const void* ptr, int64_t ld) {
