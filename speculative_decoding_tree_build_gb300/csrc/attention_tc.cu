@@ -20,7 +20,9 @@
 //     against the node's ancestor bit row. One CTA per SM, warp-specialised:
 //       warp 0      TMA producer: Q tiles, then K and V 16-row pages (4-D
 //                   tensor maps over the paged pools, 128-byte swizzle)
-//       warp 2      idle (keeps the softmax warps on their lane quarters)
+//       warp 2      prefetches the first prompt K/V pages into L2 while the
+//                   pre-pass finishes, then idles (it keeps the softmax
+//                   warps on their lane quarters)
 //       warps 1, 3  MMA issuers, one per 128-row M tile: S = Q K^T (A, B in
 //                   shared memory) and O += P V (P read from Tensor Memory),
 //                   fp32 accumulators. Keys move in 64-key steps and each M
@@ -39,6 +41,8 @@
 //     this grid merges them (log-sum-exp), many CTAs and loads in flight.
 //  Launches 2 and 3 use programmatic dependent launch so their prologues
 //  overlap the previous grid's tail. No CTA ever waits for another CTA.
+#include <algorithm>
+
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -74,7 +78,7 @@ struct TcParams {
   int32_t* tasks;        // kTaskInts per CTA: the split unit this CTA starts (merge work)
   uint8_t* partials;     // two slots of kSlotBytes(D) per CTA
   int32_t* status_rw;
-  int batch, max_nodes, t_cap, hq, hkv, group, npq, words, max_blocks, grid;   // npq = 32 / G nodes per quarter
+  int batch, max_nodes, t_cap, hq, hkv, group, npq, words, max_blocks, num_blocks, grid;   // npq = 32 / G nodes per quarter
   float scale_log2;
 };
 
@@ -339,9 +343,11 @@ __device__ __forceinline__ int tc_cta_of(long long total, int grid, long long t)
   return static_cast<int>(rem + (t - big) / q);
 }
 
-// Segment of this CTA's tile range that starts at global tile t.
+// Segment of this CTA's tile range that starts at global tile t. Without
+// `use_status` only the geometry is known (skip stays false): the form that
+// may run before the dependency wait, since the pre-pass writes status.
 __device__ TcSeg tc_segment(const TcParams& p, const int* s_pre, long long t, long long s,
-                            long long e) {
+                            long long e, bool use_status = true) {
   TcSeg g;
   g.valid = t < e;
   if (!g.valid) return g;
@@ -351,7 +357,7 @@ __device__ TcSeg tc_segment(const TcParams& p, const int* s_pre, long long t, lo
     if (s_pre[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const int st = p.status[b];            // loaded together with the request's shape
+  const int st = use_status ? p.status[b] : 0;   // loaded together with the request's shape
   const TcShape r = tc_shape(p, b);
   const long long local = t - s_pre[b];
   const int unit = static_cast<int>(local / r.tiles);
@@ -525,15 +531,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
   tc_plan_prefix(p, s_pre, s_tmp);        // contains __syncthreads; reads only call inputs
   tc_fence_after();
-  grid_launch_dependents();               // the merge grid may start its prologue
-  grid_dependency_wait();                 // rotated q, tentative KV and status are written
-  const uint32_t tbase = s_tmem;
-  volatile int* abort = &s_abort;
   const long long total = s_pre[p.batch];
   const long long cs = tc_cta_start(total, p.grid, blockIdx.x);
   const long long ce = tc_cta_start(total, p.grid, blockIdx.x + 1);
   const int G = p.group, npq = p.npq;
   const int32_t* table_base = p.block_table;
+  if (warp == 2) {
+    // While the pre-pass finishes, the otherwise idle warp pulls the prompt
+    // K/V pages of this CTA's first steps into L2 (the producer warp goes
+    // straight on to its Q and K/V copies). The pre-pass writes only the
+    // tree's slots (from P on), rotated q and status; the block table and the
+    // prompt pages were complete before it started, so they may be read
+    // before the wait. The same table entries then sit in L1 for the producer.
+    const TcSeg g = tc_segment(p, s_pre, cs, cs, ce, false);
+    if (g.valid) {
+      const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
+      const int nh = min(tc_steps(g), kTcStages);
+      for (int j = 0; j < nh; ++j) {
+        const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
+        // stop at the tree's slots, and within the request's table row (an
+        // oversized prompt is flagged only by the pre-pass)
+        if (k0 + kTcBK > g.plen || (k0 + kTcBK) / TV_BLOCK_SIZE > p.max_blocks) break;
+        if (lane < kTcBK / TV_BLOCK_SIZE) {
+          const int blk = __ldg(trow + k0 / TV_BLOCK_SIZE + lane);
+          if (blk >= 0 && blk < p.num_blocks) {
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) {
+              tma_prefetch_4d(&p.kmap, h * 64, 0, g.kvh, blk);
+              tma_prefetch_4d(&p.vmap, h * 64, 0, g.kvh, blk);
+            }
+          }
+        }
+      }
+    }
+  }
+  grid_launch_dependents();               // the merge grid may start its prologue
+  grid_dependency_wait();                 // rotated q, tentative KV and status are written
+  const uint32_t tbase = s_tmem;
+  volatile int* abort = &s_abort;
 
   if (warp == 0) {
     // ================================================= TMA producer
@@ -890,31 +925,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 // partial (normalised o_c = O_c / l_c, reference max m_c, sum l_c, per row)
 // per contributor. The merge is the usual log-sum-exp combination:
 //   out = sum_c w_c o_c / sum_c w_c,  w_c = 2^(m_c - M) l_c,  M = max_c m_c.
-// kMergeSplit CTAs per split unit, one per quarter of its rows (32 rows, 8
-// threads per row); each thread loads kMergeChunk contributors at once.
+// A work item is one quarter of a split unit's rows (32 rows, 8 threads per
+// row); each thread loads kMergeChunk contributors at once. The grid is one
+// resident wave: every CTA reads all task flags at once, lists the valid
+// records in shared memory, and takes items blockIdx.x, + gridDim.x, ...
+// of that list, so the work spreads evenly whatever records are empty.
 
 struct MergeParams {
   const int32_t* tasks;
   const uint8_t* partials;
   __nv_bfloat16* out;
   int hq, group;
+  int ntask;            // task records: one per attention CTA
 };
 
 constexpr int kMergeThreads = 256;
 constexpr int kMergeSplit = 8;      // CTAs per unit: one per row quarter
-constexpr int kMergeChunk = 4;      // contributors whose loads are in flight together
+constexpr int kMergeChunk = 2;      // contributors whose loads are in flight together
+constexpr int kMergeMinBlocks = 4;  // resident merge CTAs per SM the register budget allows
+constexpr int kMergeMaxTasks = 1024;
 
 __device__ __forceinline__ float2 half2_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
+// Row quarter j of the split unit described by task record rec.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ MergeParams p) {
-  grid_dependency_wait();            // the attention grid's partials and tasks are visible
-  grid_launch_dependents();
-  const int c = blockIdx.x / kMergeSplit, j = blockIdx.x % kMergeSplit;
-  const int32_t* rec = p.tasks + c * kTaskInts;
-  if (rec[0] == 0) return;
+__device__ __forceinline__ void merge_one(const MergeParams& p, const int32_t* rec, int j) {
   const int kvh = rec[2], node0 = rec[3], mt = rec[4], t0 = rec[5];
   const int c_first = rec[7], c_last = rec[8], first_slot = rec[9], nodes = rec[10];
   if ((j >> 2) >= mt) return;
@@ -988,6 +1025,32 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_
   for (int v = 0; v < kVecs; ++v)
     dst[v] = make_uint4(pack_bf16x2(acc[v][0] * inv, acc[v][1] * inv), pack_bf16x2(acc[v][2] * inv, acc[v][3] * inv),
                         pack_bf16x2(acc[v][4] * inv, acc[v][5] * inv), pack_bf16x2(acc[v][6] * inv, acc[v][7] * inv));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks)
+    attn_merge_kernel(const __grid_constant__ MergeParams p) {
+  __shared__ int s_list[kMergeMaxTasks];
+  __shared__ int s_wsum[kMergeThreads / 32];
+  grid_dependency_wait();            // the attention grid's partials and tasks are visible
+  grid_launch_dependents();
+  // compact the valid task records (in record order), one flag per thread
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int nvalid = 0;
+  for (int base = 0; base < p.ntask; base += kMergeThreads) {
+    const int c = base + threadIdx.x;
+    const bool v = c < p.ntask && __ldcg(p.tasks + static_cast<size_t>(c) * kTaskInts) != 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) s_wsum[warp] = __popc(bal);
+    __syncthreads();
+    int before = nvalid;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    if (v) s_list[before + __popc(bal & ((1u << lane) - 1u))] = c;
+    for (int w = 0; w < kMergeThreads / 32; ++w) nvalid += s_wsum[w];
+    __syncthreads();
+  }
+  for (int k = blockIdx.x; k < nvalid * kMergeSplit; k += gridDim.x)
+    merge_one<D>(p, p.tasks + static_cast<size_t>(s_list[k / kMergeSplit]) * kTaskInts, k % kMergeSplit);
 }
 
 // ------------------------------------------------------------ host
@@ -1121,6 +1184,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   tp.npq = L.npq;
   tp.words = (max_nodes + 31) / 32;
   tp.max_blocks = max_blocks;
+  tp.num_blocks = num_blocks;
   tp.grid = grid;
   const double scale = geom->softmax_scale > 0.f ? geom->softmax_scale : 1.0 / sqrt(double(D));
   tp.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
@@ -1131,6 +1195,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   mp.out = tp.out;
   mp.hq = hq;
   mp.group = group;
+  mp.ntask = grid;
 
   const dim3 rgrid((max_nodes + kRopeNodes - 1) / kRopeNodes, batch);
   static size_t smem_set128[kMaxDevices] = {0}, smem_set64[kMaxDevices] = {0};
@@ -1154,8 +1219,22 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   acfg.stream = stream;
   acfg.attrs = pdl;
   acfg.numAttrs = 1;
+  // the merge grid: one resident wave (never more CTAs than there can be
+  // work items)
+  static int merge_per_sm[2][kMaxDevices] = {{0}};
+  int& mps = merge_per_sm[D == 128 ? 0 : 1][dev];
+  if (mps == 0) {
+    int n = 0;
+    const cudaError_t oe = D == 128
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_merge_kernel<128>, kMergeThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_merge_kernel<64>, kMergeThreads, 0);
+    mps = (oe == cudaSuccess && n > 0) ? n : 1;
+  }
+  const int sms = device_sm_count(dev);
+  if (grid > kMergeMaxTasks) return TV_ERR_BAD_SIZE;            // one task record per CTA
+  const int mgrid = std::max(1, std::min(grid * kMergeSplit, std::max(sms, 1) * mps));
   cudaLaunchConfig_t mcfg = acfg;
-  mcfg.gridDim = dim3(grid * kMergeSplit);
+  mcfg.gridDim = dim3(mgrid);
   mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
   cudaError_t err;
