@@ -17,7 +17,7 @@ Draft Trees":
   * §6-§7.1: the tree is flattened depth by depth after the root b (position
     id = depth), e.g. [b, A, B, B, A, B, C] with positions [0, 1, 1, 2, 2, 2, 3].
 
-Readings where the pages leave a step open (listed in the design doc as well):
+Readings where the pages leave a step open:
   * ranks order a position's tokens by logit descending, equal logits by
     token id ascending;
   * log q_i(v) = h_i(v) - logsumexp(h_i), in float64 here; a position whose

@@ -13,7 +13,7 @@ Candidates are given in generation order (a candidate's parent comes before
 it): per candidate the drafter's log-probability of its token under its
 parent, its parent candidate (-1 for the root's children) and its token.
 
-Readings where the pages leave a step open (listed in the design doc as well):
+Readings where the pages leave a step open:
   * the score of a candidate is its parent's score plus its own
     log-probability (log of the survival product), evaluated in float32 in
     that order - the precision the CUDA kernel decides in, so equal inputs give

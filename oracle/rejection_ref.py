@@ -11,7 +11,7 @@ whole path is accepted the bonus token is sampled at the last node's next
 position. "解码：采样、束搜索和推测性解码" ("Gumbel Max技巧") gives the
 sampler: argmax_v (log w_v + g_v) draws from w / sum(w).
 
-Readings where the pages leave a step open (listed in the design doc as well):
+Readings where the pages leave a step open:
   * the path goes from the root to the leaf with the largest cumulative draft
     log-probability (sum of the draft log-probabilities of its tokens), the
     smallest node index on ties, a NaN sum counting as -inf;

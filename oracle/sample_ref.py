@@ -14,7 +14,7 @@ Definitions followed:
     lossless: its output follows the target's own autoregressive sampling).
   * "02 · Token Tree 与 Tree Attention" §4 (the greedy rule compares token ids).
 
-Readings where the pages leave a step open (listed in the design doc as well):
+Readings where the pages leave a step open:
   * temperature T divides the logits; T == 0 means greedy (argmax of the raw
     logits);
   * the noise g is an input, one float32 value per (node, vocabulary entry),

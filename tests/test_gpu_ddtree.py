@@ -132,7 +132,7 @@ def _scores_by_prefix(logq):
 
 
 def test_chained_topk_and_build_from_logits():
-    """Config 4's recipe: 16 requests, L = 16, vocabulary 151936, N(0, 3)
+    """The DDTree workload's recipe: 16 requests, L = 16, vocabulary 151936, N(0, 3)
     logits, budget 256; the chained GPU result against the oracle from the
     same logits, then fed to tv_tree_build."""
     rng = np.random.default_rng(44)
