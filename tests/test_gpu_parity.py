@@ -156,8 +156,14 @@ def _star(n):
 
 
 @pytest.mark.parametrize("case", ["empty_prompt", "root_only", "chain_1024", "star_300",
-                                  "block_edges", "group16_d64_halfsplit"])
+                                  "block_edges", "group16_d64_halfsplit", "tail_g1_16_nodes",
+                                  "tail_g16_d64_one_node", "tail_g8_halfsplit"])
 def test_attention_edge_cases(case):
+    """Degenerate and boundary shapes. The tail_* cases end a KV head's query
+    rows with a unit of at most 16 rows after full 256-row units: 16 nodes of
+    one head, one node of 16 heads, and 8-head groups of one and two nodes,
+    with prompts long enough that those units are also split between CTAs
+    and merged."""
     if case == "empty_prompt":
         w = _custom(wl.GEOM_8B, [wl.medusa_tree(np.random.default_rng(1), (4, 3), 100)] * 2, [0, 0])
     elif case == "root_only":
@@ -170,6 +176,14 @@ def test_attention_edge_cases(case):
         rng = np.random.default_rng(3)
         trees = [wl.eagle_tree(rng, 4, 3, 20, 1000)[:2] for _ in range(5)]
         w = _custom(wl.GEOM_8B, trees, [15, 16, 63, 64, 65])
+    elif case == "tail_g1_16_nodes":
+        w = _custom(wl.Geometry(2, 2, 128), [_star(272), _chain(272)], [3, 700], max_nodes=272)
+    elif case == "tail_g16_d64_one_node":
+        w = _custom(wl.Geometry(16, 1, 64), [_star(17), _chain(17), _star(17)], [0, 40, 1333])
+    elif case == "tail_g8_halfsplit":
+        rng = np.random.default_rng(5)
+        trees = [wl.eagle_tree(rng, 4, 4, 32, 1000)[:2], _star(34), _chain(33)]
+        w = _custom(wl.Geometry(64, 8, 128, rope_style=1), trees, [500, 1000, 77])
     else:
         geom = wl.Geometry(16, 1, 64, rope_style=1)
         rng = np.random.default_rng(4)
