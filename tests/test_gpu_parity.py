@@ -36,6 +36,7 @@ def _check_step(w, db_pre_k, db_pre_v, db, ref, pairs=None):
     check_tree_outputs(db, ref, w)
     compare_out(db.out_f32(), ref["out"], w, pairs)
     cu = w["cu_nodes"]
+    k_diff = k_total = 0
     for b in range(w["batch"]):
         if ref["status"][b]:
             continue
@@ -46,7 +47,13 @@ def _check_step(w, db_pre_k, db_pre_v, db, ref, pairs=None):
         assert np.array_equal(got_v, w["v_new"][cu[b]:cu[b + 1]])
         rope_close(got_k, bf16_bits_to_f64(w["k_new"][cu[b]:cu[b + 1]]),
                    ref["positions"][cu[b]:cu[b + 1]], w)
-        assert np.mean(bf16_ulp_diff(got_k, want_k) > 0) < 1e-3
+        d = bf16_ulp_diff(got_k, want_k)
+        k_diff += int(np.count_nonzero(d))
+        k_total += d.size
+    # last-bit differences (float32 rotation vs exact) are rare rounding
+    # boundaries: counted over the batch, since a one-node request has too
+    # few elements for a per-request rate
+    assert k_total == 0 or k_diff / k_total < 1e-3
     check_accept_outputs(db, ref, w)
     # commit: the GPU's own pre-commit pool with the oracle's path applied
     k_exp, v_exp = db_pre_k.copy(), db_pre_v.copy()
@@ -157,13 +164,17 @@ def _star(n):
 
 @pytest.mark.parametrize("case", ["empty_prompt", "root_only", "chain_1024", "star_300",
                                   "block_edges", "group16_d64_halfsplit", "tail_g1_16_nodes",
-                                  "tail_g16_d64_one_node", "tail_g8_halfsplit"])
+                                  "tail_g16_d64_one_node", "tail_g8_halfsplit", "batch_4096_roots",
+                                  "many_tiny_trees"])
 def test_attention_edge_cases(case):
     """Degenerate and boundary shapes. The tail_* cases end a KV head's query
     rows with a unit of at most 16 rows after full 256-row units: 16 nodes of
     one head, one node of 16 heads, and 8-head groups of one and two nodes,
     with prompts long enough that those units are also split between CTAs
-    and merged."""
+    and merged. batch_4096_roots is the largest batch the library takes (one
+    root node each, prompts of 0-16 tokens: the work plan's prefix over the
+    batch at its largest); many_tiny_trees gives every CTA dozens of
+    one-tile units in a row."""
     if case == "empty_prompt":
         w = _custom(wl.GEOM_8B, [wl.medusa_tree(np.random.default_rng(1), (4, 3), 100)] * 2, [0, 0])
     elif case == "root_only":
@@ -180,6 +191,14 @@ def test_attention_edge_cases(case):
         w = _custom(wl.Geometry(2, 2, 128), [_star(272), _chain(272)], [3, 700], max_nodes=272)
     elif case == "tail_g16_d64_one_node":
         w = _custom(wl.Geometry(16, 1, 64), [_star(17), _chain(17), _star(17)], [0, 40, 1333])
+    elif case == "batch_4096_roots":
+        rng = np.random.default_rng(11)
+        w = _custom(wl.Geometry(4, 2, 64), [([-1], [int(x)]) for x in rng.integers(0, 100, 4096)],
+                    list(rng.integers(0, 17, 4096)))
+    elif case == "many_tiny_trees":
+        rng = np.random.default_rng(12)
+        trees = [wl.eagle_tree(rng, 2, 3, int(rng.integers(1, 6)), 1000)[:2] for _ in range(1500)]
+        w = _custom(wl.Geometry(8, 2, 128), trees, list(rng.integers(0, 200, 1500)))
     elif case == "tail_g8_halfsplit":
         rng = np.random.default_rng(5)
         trees = [wl.eagle_tree(rng, 4, 4, 32, 1000)[:2], _star(34), _chain(33)]
