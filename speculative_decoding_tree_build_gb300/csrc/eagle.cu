@@ -18,9 +18,12 @@
 //    shallower, then earlier generated), keeps the first n_keep, checks they
 //    are prefix-closed and packs them breadth first (depth, parent's packed
 //    index, generation order) into a parent list for tv_tree_build.
-// Ranks are counts of larger keys (each thread ranks its candidates against
-// all others in shared memory): exact, order-independent and free of sorting
-// networks at these sizes (a few hundred to a few thousand candidates).
+// Ranks are counts of larger keys in shared memory: exact, order-independent
+// and free of sorting networks at these sizes (a few hundred to a few
+// thousand candidates). Every thread takes part: a candidate's comparisons
+// are split over several threads whose partial counts meet in shared
+// memory. The breadth-first packing works on the kept nodes only, gathered
+// by their (unique) global rank.
 #include "tv_common.cuh"
 
 namespace tv {
@@ -77,6 +80,29 @@ __device__ int eagle_stage(const float* logp, const int32_t* parent, int m, Eagl
   return 0;
 }
 
+
+// rank[i] = number of keys larger than key[i], i < n (keys are distinct).
+// All threads call it. With fewer keys than threads, each key's comparisons
+// are split over up to 32 threads.
+__device__ void eagle_rank(const uint64_t* key, int n, int* rank) {
+  const int nt = blockDim.x;
+  const int slices = n >= nt ? 1 : min(32, nt / max(n, 1));
+  for (int i = threadIdx.x; i < n; i += nt) rank[i] = 0;
+  __syncthreads();
+  const int work = n * slices;
+  for (int w = threadIdx.x; w < work; w += nt) {
+    const int i = w % n, sl = w / n;
+    const int j0 = static_cast<int>(static_cast<long long>(n) * sl / slices);
+    const int j1 = static_cast<int>(static_cast<long long>(n) * (sl + 1) / slices);
+    const uint64_t ki = key[i];
+    int cnt = 0;
+    for (int j = j0; j < j1; ++j) cnt += key[j] > ki ? 1 : 0;
+    if (slices == 1) rank[i] = cnt;
+    else if (cnt) atomicAdd(&rank[i], cnt);
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kEagleThreads)
 eagle_expand_select_kernel(const float* __restrict__ logp, const int32_t* __restrict__ parent,
                            const int32_t* __restrict__ cand_count, int max_cands, int layer,
@@ -100,22 +126,26 @@ eagle_expand_select_kernel(const float* __restrict__ logp, const int32_t* __rest
     if (threadIdx.x == 0) atomicOr(&status[b], flags);
     return;
   }
+  uint64_t* key = reinterpret_cast<uint64_t*>(lp + kEagleMaxCands);    // [max_cands]
+  int* lc = reinterpret_cast<int*>(key + kEagleMaxCands);               // the layer's candidates
+  int* rank = reinterpret_cast<int*>(lp);                               // log-probs no longer needed
+  __shared__ int s_nl;
   int32_t* out = selected + static_cast<size_t>(b) * k;
   for (int r = threadIdx.x; r < k; r += blockDim.x) out[r] = -1;
+  if (threadIdx.x == 0) s_nl = 0;
   __syncthreads();
+  // the layer's candidates (in any order: the key carries the generation index)
   for (int c = threadIdx.x; c < m; c += blockDim.x) {
     if (s.depth[c] != layer) continue;
-    const uint64_t key = (static_cast<uint64_t>(eagle_float_key(s.score[c])) << 32) |
-                         static_cast<uint32_t>(~c);
-    int rank = 0;
-    for (int j = 0; j < m; ++j) {
-      if (s.depth[j] != layer) continue;
-      const uint64_t kj = (static_cast<uint64_t>(eagle_float_key(s.score[j])) << 32) |
-                          static_cast<uint32_t>(~j);
-      rank += kj > key;
-    }
-    if (rank < k) out[rank] = c;
+    const int i = atomicAdd(&s_nl, 1);
+    lc[i] = c;
+    key[i] = (static_cast<uint64_t>(eagle_float_key(s.score[c])) << 32) | static_cast<uint32_t>(~c);
   }
+  __syncthreads();
+  const int nl = s_nl;
+  eagle_rank(key, nl, rank);
+  for (int i = threadIdx.x; i < nl; i += blockDim.x)
+    if (rank[i] < k) out[rank[i]] = lc[i];
 }
 
 __global__ void __launch_bounds__(kEagleThreads)
@@ -129,6 +159,10 @@ eagle_rerank_kernel(const float* __restrict__ logp, const int32_t* __restrict__ 
   float* lp = reinterpret_cast<float*>(smem + sizeof(EagleSmem));      // [max_cands]
   int* packed = reinterpret_cast<int*>(lp + kEagleMaxCands);           // [max_cands]
   int* start = packed + kEagleMaxCands;                                // [kEagleMaxCands + 2]
+  uint64_t* key = reinterpret_cast<uint64_t*>(start + kEagleMaxCands + 2);  // [max_cands]
+  int* kn = reinterpret_cast<int*>(key + kEagleMaxCands);              // kept nodes by rank
+  int* ppk = kn + TV_MAX_NODES;                                        // parent's packed index
+  int* rank = reinterpret_cast<int*>(lp);                              // log-probs no longer needed
   __shared__ int s_maxd;
   grid_dependency_wait();
   grid_launch_dependents();
@@ -153,20 +187,17 @@ eagle_rerank_kernel(const float* __restrict__ logp, const int32_t* __restrict__ 
   }
   for (int i = threadIdx.x; i < kEagleMaxCands + 2; i += blockDim.x) start[i] = 0;
   if (threadIdx.x == 0) s_maxd = 0;
-  __syncthreads();
   // global rank: score descending, then shallower, then earlier generated
+  for (int c = threadIdx.x; c < m; c += blockDim.x)
+    key[c] = (static_cast<uint64_t>(eagle_float_key(s.score[c])) << 32) |
+             static_cast<uint32_t>(~((static_cast<uint32_t>(s.depth[c]) << 12) | c));
+  __syncthreads();
+  eagle_rank(key, m, rank);
   for (int c = threadIdx.x; c < m; c += blockDim.x) {
-    const uint64_t key = (static_cast<uint64_t>(eagle_float_key(s.score[c])) << 32) |
-                         static_cast<uint32_t>(~((static_cast<uint32_t>(s.depth[c]) << 12) | c));
-    int rank = 0;
-    for (int j = 0; j < m; ++j) {
-      const uint64_t kj = (static_cast<uint64_t>(eagle_float_key(s.score[j])) << 32) |
-                          static_cast<uint32_t>(~((static_cast<uint32_t>(s.depth[j]) << 12) | j));
-      rank += kj > key;
-    }
-    const bool kept = rank < n_keep;
+    const bool kept = rank[c] < n_keep;
     packed[c] = kept ? -2 : -1;
     if (kept) {
+      kn[rank[c]] = c;
       atomicAdd(&start[s.depth[c] + 1], 1);
       atomicMax(&s_maxd, s.depth[c]);
     }
@@ -187,25 +218,27 @@ eagle_rerank_kernel(const float* __restrict__ logp, const int32_t* __restrict__ 
     for (int d = 2; d <= maxd; ++d) start[d] += start[d - 1];
   }
   __syncthreads();
-  // breadth first: level by level, by (parent's packed index, generation
-  // order); the level's new indices go to a side array so that the ranking
-  // reads a stable `packed`
-  int* level_pk = reinterpret_cast<int*>(lp);              // log-probs are no longer needed
+  // breadth first over the kept nodes, level by level, by (parent's packed
+  // index, generation order): first every kept node of the level notes its
+  // parent's packed index (the parents' level is final), then each ranks
+  // itself among them
   for (int d = 1; d <= maxd; ++d) {
-    for (int c = threadIdx.x; c < m; c += blockDim.x) {
-      if (packed[c] != -2 || s.depth[c] != d) continue;
-      const int pc = s.parent[c] < 0 ? 0 : packed[s.parent[c]];
-      int rank = 0;
-      for (int j = 0; j < m; ++j) {
-        if (packed[j] != -2 || s.depth[j] != d) continue;
-        const int pj = s.parent[j] < 0 ? 0 : packed[s.parent[j]];
-        rank += (pj < pc) || (pj == pc && j < c);
-      }
-      level_pk[c] = start[d] + rank;
+    for (int i = threadIdx.x; i < n_keep; i += blockDim.x) {
+      const int c = kn[i];
+      ppk[i] = s.depth[c] != d ? -1 : s.parent[c] < 0 ? 0 : packed[s.parent[c]];
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < m; c += blockDim.x)
-      if (packed[c] == -2 && s.depth[c] == d) packed[c] = level_pk[c];
+    for (int i = threadIdx.x; i < n_keep; i += blockDim.x) {
+      const int pc = ppk[i];
+      if (pc < 0) continue;
+      const int c = kn[i];
+      int r = 0;
+      for (int j = 0; j < n_keep; ++j) {
+        const int pj = ppk[j];
+        r += (pj >= 0 && (pj < pc || (pj == pc && kn[j] < c))) ? 1 : 0;
+      }
+      packed[c] = start[d] + r;
+    }
     __syncthreads();
   }
   const size_t out0 = static_cast<size_t>(b) * n_out;
@@ -222,10 +255,13 @@ eagle_rerank_kernel(const float* __restrict__ logp, const int32_t* __restrict__ 
   }
 }
 
-static size_t expand_smem_bytes() { return sizeof(EagleSmem) + kEagleMaxCands * sizeof(float); }
+static size_t expand_smem_bytes() {
+  return sizeof(EagleSmem) + kEagleMaxCands * (sizeof(float) + sizeof(uint64_t) + sizeof(int));
+}
 static size_t rerank_smem_bytes() {
   return sizeof(EagleSmem) + kEagleMaxCands * (sizeof(float) + sizeof(int)) +
-         (kEagleMaxCands + 2) * sizeof(int);
+         (kEagleMaxCands + 2) * sizeof(int) + kEagleMaxCands * sizeof(uint64_t) +
+         2 * TV_MAX_NODES * sizeof(int);
 }
 
 }  // namespace tv
