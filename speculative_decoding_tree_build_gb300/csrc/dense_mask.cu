@@ -10,15 +10,16 @@
 // Input: the bit-packed rows of tv_tree_build. Output, request after request
 // (row-major, no padding): FULL_MASK [N_b][P_b + N_b], QLEN_ONLY [N_b][N_b];
 // elements uint8 (1 visible, 0 masked) or float32 (0 visible, -inf masked).
-// One CTA writes ROWS rows of one request; each thread writes whole 16-byte
-// groups of the output (the row edges, which need not be 16-byte aligned,
-// are written with narrower stores). Write-bandwidth-bound.
+// One CTA writes kMaskRows rows of one request, one warp per row; each lane
+// writes whole 16-byte groups of its row (the row edges, which need not be
+// 16-byte aligned, are written with narrower stores). Write-bandwidth-bound
+// for long rows, latency-bound at the sizes of one verification step.
 #include "tv_common.cuh"
 
 namespace tv {
 
 constexpr int kMaskThreads = 256;
-constexpr int kMaskRows = 8;
+constexpr int kMaskRows = kMaskThreads / 32;     // one warp per row
 
 // Elements before request b's block: sum over earlier requests of N (P + N)
 // (or N * N), reduced by the whole CTA.
@@ -61,7 +62,9 @@ tree_mask_dense_kernel(const uint32_t* __restrict__ mask_bits, const int32_t* __
   if (status[b] != 0 || n <= 0) return;
   const long long width = static_cast<long long>(p) + n;
   constexpr int kVec = 16 / sizeof(T);                     // elements per 16-byte group
-  for (int r = blockIdx.x * kMaskRows; r < min(n, (blockIdx.x + 1) * kMaskRows); ++r) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kMaskRows + static_cast<int>(threadIdx.x >> 5);
+  if (r < n) {
     const uint32_t* bits = mask_bits + static_cast<size_t>(t0 + r) * words;
     T* row = out + base + static_cast<long long>(r) * width;
     // element e of the row is visible iff e < p, or bit (e - p) of the row
@@ -73,9 +76,9 @@ tree_mask_dense_kernel(const uint32_t* __restrict__ mask_bits, const int32_t* __
     // head up to the first 16-byte boundary, aligned body, tail
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
     const long long head = min(width, static_cast<long long>(((16 - (addr & 15)) & 15) / sizeof(T)));
-    for (long long e = threadIdx.x; e < head; e += blockDim.x) row[e] = value(e);
+    for (long long e = lane; e < head; e += 32) row[e] = value(e);
     const long long body = (width - head) / kVec;
-    for (long long g = threadIdx.x; g < body; g += blockDim.x) {
+    for (long long g = lane; g < body; g += 32) {
       const long long e0 = head + g * kVec;
       union { uint4 v; T x[kVec]; } u;
       if (e0 + kVec <= p) {
@@ -87,7 +90,7 @@ tree_mask_dense_kernel(const uint32_t* __restrict__ mask_bits, const int32_t* __
       }
       *reinterpret_cast<uint4*>(row + e0) = u.v;
     }
-    for (long long e = head + body * kVec + threadIdx.x; e < width; e += blockDim.x) row[e] = value(e);
+    for (long long e = head + body * kVec + lane; e < width; e += 32) row[e] = value(e);
   }
 }
 
