@@ -57,9 +57,10 @@ def build(force=False, verbose_ptxas=False, quiet=True):
     os.makedirs(BUILD, exist_ok=True)
     stamp_path = os.path.join(BUILD, "stamp")
     stamp = _stamp(extra)
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_path)
-            and open(stamp_path).read() == stamp):
-        return LIB
+    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+        with open(stamp_path) as fh:
+            if fh.read() == stamp:
+                return LIB
     nvcc = _nvcc()
     objs = []
 

@@ -24,7 +24,8 @@ def header_functions():
     names = []
     for f in os.listdir(os.path.join(ROOT, "include")):
         if f.endswith(".h"):
-            text = open(os.path.join(ROOT, "include", f), encoding="utf-8").read()
+            with open(os.path.join(ROOT, "include", f), encoding="utf-8") as fh:
+                text = fh.read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tv_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
@@ -188,8 +189,9 @@ def test_fma_exp2_cubic_error_bound():
     x = j + f with j = rint(x) reproduces 2^x on the kernel's input range."""
     import numpy as np
 
-    src = open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", "attention_tc.cu"),
-               encoding="utf-8").read()
+    with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", "attention_tc.cu"),
+              encoding="utf-8") as fh:
+        src = fh.read()
     body = src[src.index("float exp2_fma(float x)"):]
     body = body[:body.index("}")]
     coefs = [float(c) for c in re.findall(r"([0-9]\.[0-9]+e[-+][0-9]+)f", body)]
