@@ -76,6 +76,8 @@ extern "C" int tv_accept_commit(const tv_geom* geom, const int32_t* target_ids,
                                 void* stream) {
   int rc = tv::check_geom(geom);
   if (rc != TV_OK) return rc;
+  rc = tv::check_commit_geom(geom, tv::kFusedStage);
+  if (rc != TV_OK) return rc;
   if (batch < 0 || max_nodes < 1 || max_nodes > TV_MAX_NODES || max_depth < 0 ||
       max_blocks_per_req < 1 || num_blocks < 1)
     return TV_ERR_BAD_SIZE;

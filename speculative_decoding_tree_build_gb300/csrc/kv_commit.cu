@@ -68,6 +68,8 @@ extern "C" int tv_kv_commit(const tv_geom* geom, int32_t batch, const int32_t* a
                             int32_t* released_count, int32_t* status, void* stream) {
   int rc = tv::check_geom(geom);
   if (rc != TV_OK) return rc;
+  rc = tv::check_commit_geom(geom, tv::kCommitSmem);
+  if (rc != TV_OK) return rc;
   if (batch < 0 || max_depth < 0 || max_blocks_per_req < 1 || num_blocks < 1)
     return TV_ERR_BAD_SIZE;
   if (batch == 0) return TV_OK;

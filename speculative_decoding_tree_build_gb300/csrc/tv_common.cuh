@@ -77,6 +77,14 @@ inline int check_geom(const tv_geom* g) {
   return TV_OK;
 }
 
+// The commit kernels move accepted rows through a shared-memory staging
+// buffer of stage_bytes, whole K+V rows (all KV heads) at a time; a geometry
+// whose one row does not fit cannot be committed.
+inline int check_commit_geom(const tv_geom* g, int stage_bytes) {
+  const long long row_bytes = 2ll * g->num_kv_heads * g->head_dim * 2;
+  return row_bytes <= stage_bytes ? TV_OK : TV_ERR_BAD_GEOMETRY;
+}
+
 // --------------------------------------------------------------- device side
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

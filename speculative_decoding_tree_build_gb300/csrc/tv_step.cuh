@@ -107,6 +107,7 @@ __device__ __forceinline__ int commit_rows(const int* path, int a, int plen, int
   // rows to move (k with path[k] == k is already in place)
   const int row_vecs = 2 * hkv * head_vecs;   // K and V, all heads
   const int chunk_rows = stage_bytes / (row_vecs * 16);
+  if (chunk_rows < 1) return TV_ST_BAD_SIZE;   // a row larger than the stage (the host rejects it)
   for (int k0 = 1; k0 <= a; k0 += chunk_rows) {
     const int k1 = min(a + 1, k0 + chunk_rows);
     const int total = (k1 - k0) * row_vecs;
