@@ -24,10 +24,9 @@ Readings where the pages leave a step open:
     logits are all -inf gives -inf for every token;
   * a pushed tuple's score is its parent prefix's score plus its own last
     log-probability (the page's sibling update sigma - log q(r) + log q(r+1)
-    is the same quantity). The heap's decisions are taken in float32: the
-    per-position log-probabilities are float32 values and each score is the
-    float32 sum of the parent's score and that value, the precision the CUDA
-    kernel decides in, so equal inputs give the same tree bit for bit;
+    is the same quantity), summed in float64 from the per-position values
+    (the page fixes no precision; float64 is the plain reading of "the sum
+    of the log-probabilities");
   * equal scores pop the shallower tuple first, then the one whose parent
     popped earlier, then the smaller last rank;
   * output order: the root, then depth by depth, pop order within a depth;
@@ -64,31 +63,29 @@ def topk_logprobs_ref(logits, k):
 def ddtree_build_ref(logq, tokens, budget, root_token=-1):
     """Algorithm 1 over rank tuples.
 
-    logq [L][K] per-depth log-probabilities in rank order (rounded to float32
-    for the decisions), tokens [L][K] the matching token ids. Returns (parents,
+    logq [L][K] per-depth log-probabilities in rank order (any float type; used
+    as float64), tokens [L][K] the matching token ids. Returns (parents,
     node_tokens, depths, scores, pops) with node 0 the root; ``pops`` lists the
     popped rank tuples (1-based ranks) in pop order."""
-    lq = np.asarray(logq, dtype=np.float32)
+    lq = np.asarray(logq, dtype=np.float64)
     L, K = lq.shape
-    f32 = np.float32
     # heap entries: (-score, depth, parent pop index, last rank, tuple)
-    heap = [(-float(lq[0, 0]), 1, 0, 1, (1,))]
+    heap = [(-lq[0, 0], 1, 0, 1, (1,))]
     pop_index = {(): 0}                  # root counts as popped first
     pops, scores = [], []
     while heap and len(pops) < budget:
         neg, d, _, r, rho = heapq.heappop(heap)
-        sigma = f32(-neg)
+        sigma = -neg
         pops.append(rho)
         scores.append(sigma)
         pop_index[rho] = len(pops)
         parent = rho[:-1]
-        parent_score = f32(0.0) if d == 1 else scores[pop_index[parent] - 1]
+        parent_score = 0.0 if d == 1 else scores[pop_index[parent] - 1]
         if r + 1 <= K:                                   # next sibling
-            s = f32(parent_score + lq[d - 1, r])
-            heapq.heappush(heap, (-float(s), d, pop_index[parent], r + 1, parent + (r + 1,)))
+            heapq.heappush(heap, (-(parent_score + lq[d - 1, r]), d, pop_index[parent], r + 1,
+                                  parent + (r + 1,)))
         if d < L:                                        # first child
-            s = f32(sigma + lq[d, 0])
-            heapq.heappush(heap, (-float(s), d + 1, pop_index[rho], 1, rho + (1,)))
+            heapq.heappush(heap, (-(sigma + lq[d, 0]), d + 1, pop_index[rho], 1, rho + (1,)))
     # flatten: root, then by depth, pop order within a depth
     order = sorted(range(len(pops)), key=lambda j: (len(pops[j]), j))
     slot = {(): 0}
@@ -98,7 +95,7 @@ def ddtree_build_ref(logq, tokens, budget, root_token=-1):
     parents = np.full(n, -1, np.int32)
     node_tokens = np.full(n, root_token, np.int32)
     depths = np.zeros(n, np.int32)
-    node_scores = np.zeros(n, np.float32)
+    node_scores = np.zeros(n, np.float64)
     for j in order:
         rho = pops[j]
         s = slot[rho]

@@ -2,11 +2,14 @@
 
 tv_ddtree_topk: token ranks bit for bit (they are decided by comparisons of
 the input logits), log-probabilities within 1e-5 (the row's log-sum-exp is
-accumulated in float32). tv_ddtree_build: fed the oracle's own float32
-log-probabilities it must reproduce the oracle's tree bit for bit (both take
-the heap's decisions in float32). The two chained (logits -> tree) may differ
-from the oracle only where two prefix scores are within the log-sum-exp
-error; such a tree is checked to be a valid top-B."""
+accumulated in float32). tv_ddtree_build: fed the same float32
+log-probabilities as the oracle, it must give the oracle's tree, except where
+the kernel's float32 prefix sums decide between prefixes whose float64 scores
+(the oracle's) lie within float32 rounding of each other: such a tree is
+checked to be a valid top-B within that rounding bound, and the cases are
+counted and bounded. The two chained (logits -> tree) may differ from the
+oracle only where two prefix scores are within the log-sum-exp error; such a
+tree is checked the same way."""
 
 import numpy as np
 import pytest
@@ -89,6 +92,58 @@ def gpu_build(logq, toks, budget, roots=None):
     return n, par.cpu().numpy().reshape(batch, n), tok.cpu().numpy().reshape(batch, n), cu.cpu().numpy()
 
 
+def _gpu_tuples(par, tok, toks_ranked):
+    """Rank tuples (1-based ranks per depth) of a flattened tree's nodes."""
+    n = len(par)
+    depth = np.zeros(n, int)
+    tup = [()] * n
+    for i in range(1, n):
+        depth[i] = depth[par[i]] + 1
+        r = int(np.nonzero(toks_ranked[depth[i] - 1] == tok[i])[0][0]) + 1
+        tup[i] = tup[par[i]] + (r,)
+    return depth, tup
+
+
+def check_top_b_within(par, tok, logq, toks_ranked, tol):
+    """A tree that differs from the oracle's: it must still be a top-B under
+    the float64 prefix scores within ``tol`` (prefix-closed and flattened
+    depth by depth, no prefix outside it better than one inside by more than
+    tol, and pop order within a depth non-increasing up to tol)."""
+    L, K = logq.shape
+    n = len(par)
+    assert par[0] == -1 and np.all(par[1:] < np.arange(1, n))
+
+    def score(rho):
+        return float(sum(float(logq[i, r - 1]) for i, r in enumerate(rho)))
+    depth, tup = _gpu_tuples(par, tok, toks_ranked)
+    assert np.all(np.diff(depth) >= 0)
+    inside = set(tup[1:])
+    assert len(inside) == n - 1
+    sc = [score(t) for t in tup[1:]]
+    worst_in = min(sc)
+    frontier = []
+    for t in list(inside) + [()]:
+        if len(t) < L and t + (1,) not in inside:
+            frontier.append(t + (1,))
+        if t and t[-1] < K and t[:-1] + (t[-1] + 1,) not in inside:
+            frontier.append(t[:-1] + (t[-1] + 1,))
+    if frontier:
+        assert max(score(t) for t in frontier) <= worst_in + tol
+    for i in range(1, n - 1):
+        if depth[i] == depth[i + 1]:
+            assert sc[i - 1] >= sc[i] - tol
+
+
+def f32_sum_tol(logq):
+    """Bound on the difference between a float32 and a float64 sum of up to
+    L of the given values: L roundings of a partial sum no larger than the
+    largest possible prefix magnitude."""
+    L = logq.shape[0]
+    mag = np.where(np.isfinite(logq), np.abs(logq.astype(np.float64)), 0.0)
+    big = float(np.sum(np.max(mag, axis=1)))
+    return 2.0 * L * 2.0 ** -24 * (1.0 + big)
+
+
 @pytest.mark.parametrize("batch,L,V,budget,sigma", [(16, 16, 151936, 256, 3.0), (4, 3, 4, 6, 1.0),
                                                     (3, 16, 2000, 1023, 3.0), (2, 1, 500, 40, 1.0),
                                                     (5, 64, 50, 300, 0.5), (2, 4, 2, 100, 1.0),
@@ -105,10 +160,16 @@ def test_build_matches_oracle_on_oracle_logq(batch, L, V, budget, sigma):
     roots = rng.integers(0, V, size=batch)
     n, par, tok, cu = gpu_build(logq, toks, budget, roots)
     assert cu.tolist() == [b * n for b in range(batch + 1)]
+    near_ties = 0
     for b in range(batch):
         rp, rt, rd, rs, pops = ddtree_build_ref(logq[b], toks[b], budget, int(roots[b]))
         assert len(rp) == n
-        assert np.array_equal(par[b], rp) and np.array_equal(tok[b], rt), f"request {b}"
+        if np.array_equal(par[b], rp) and np.array_equal(tok[b], rt):
+            continue
+        near_ties += 1                 # float32 vs float64 prefix sums at a near-tie
+        assert tok[b][0] == roots[b]
+        check_top_b_within(par[b], tok[b], logq[b], toks[b], f32_sum_tol(logq[b]))
+    assert near_ties <= 2, f"{near_ties} of {batch} trees differ"
 
 
 def test_build_ties_and_dead_positions():
@@ -120,6 +181,8 @@ def test_build_ties_and_dead_positions():
     toks = np.tile(np.arange(k, dtype=np.int32), (2, L, 1)) + 100
     n, par, tok, cu = gpu_build(logq, toks, 200)
     for b in range(2):
+        # equal float32 values sum to the same score in float32 and float64
+        # alike here, so the tie rules alone decide: exact agreement
         rp, rt, *_ = ddtree_build_ref(logq[b], toks[b], 200)
         assert np.array_equal(par[b], rp) and np.array_equal(tok[b], rt)
 
