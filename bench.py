@@ -61,7 +61,7 @@ def workload_config(w):
         "workload": {2: "llama3-8b-attn-medusa", 3: "llama3-8b-attn-eagle2",
                      4: "llama3-70b-attn-ddtree", 5: "llama3-8b-attn-ragged-eagle",
                      1: "tiny-medusa"}.get(w["config"], str(w["config"])),
-        "description": __import__("speculative_decoding_tree_build_gb300.workloads",
+        "description": __import__("gen.workloads",
                                   fromlist=["CONFIG_NAMES"]).CONFIG_NAMES[w["config"]],
         "batch": int(w["batch"]), "num_q_heads": w["num_q_heads"],
         "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
@@ -146,7 +146,7 @@ def measure_eagle(dev, stream, flush, iters):
     import torch
 
     import speculative_decoding_tree_build_gb300 as tvb
-    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from gen import workloads as wl
 
     rng = np.random.default_rng(3003)
     batch, layers, k, keep = 32, 6, 8, 64
@@ -269,7 +269,7 @@ def measure_sampling(w, dev, stream, flush, iters, hbm_peak):
     import torch
 
     import speculative_decoding_tree_build_gb300 as tvb
-    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from gen import workloads as wl
 
     rng = np.random.default_rng(4242 + int(w["config"]))
     logits_h, gumbel_h = wl.sampling_inputs(rng, w)
@@ -351,7 +351,7 @@ def measure_rejection(w, dev, stream, flush, iters, hbm_peak):
     import torch
 
     import speculative_decoding_tree_build_gb300 as tvb
-    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from gen import workloads as wl
 
     rng = np.random.default_rng(5151 + int(w["config"]))
     logits_h, draft_h, gumbel_h, unif_h, logp_h = wl.rejection_inputs(rng, w)
@@ -578,7 +578,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from gen import workloads as wl
     w = wl.make_config(args.config)
     cores = os.cpu_count() or 1
     # each step: one request's verification on the oracle; size so the run ends in minutes
@@ -625,7 +625,7 @@ def run_ours(args):
 
     from __graft_entry__ import build
     build()
-    from speculative_decoding_tree_build_gb300 import workloads as wl
+    from gen import workloads as wl
     from speculative_decoding_tree_build_gb300.step import DeviceBatch
 
     w = wl.make_config(args.config, seed=rank_seed(args.config, rank))

@@ -36,7 +36,7 @@ def _bf16(bits, dev):
 
 
 class DeviceBatch:
-    """A workload dict (see workloads.py) resident on a CUDA device, plus the
+    """A workload dict (see gen/workloads.py) resident on a CUDA device, plus the
     output buffers and the attention workspace."""
 
     def __init__(self, w, device="cuda", workspace=None):

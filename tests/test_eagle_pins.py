@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from oracle.eagle_ref import eagle_expand_select_ref, eagle_rerank_ref, eagle_scores_ref
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 
 
 def random_candidates(rng, m):

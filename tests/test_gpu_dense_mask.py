@@ -8,7 +8,7 @@ import torch
 
 import speculative_decoding_tree_build_gb300 as tv
 from oracle import dense_tree_mask_ref
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 from speculative_decoding_tree_build_gb300.build import build
 
 pytestmark = pytest.mark.gpu

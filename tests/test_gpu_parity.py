@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from oracle import kv_commit_ref
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 from speculative_decoding_tree_build_gb300.build import build
 from speculative_decoding_tree_build_gb300.step import DeviceBatch
 

@@ -15,7 +15,7 @@ import torch
 
 import speculative_decoding_tree_build_gb300 as tv
 from oracle import chosen_path_ref, rejection_walk_ref
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 from speculative_decoding_tree_build_gb300.build import build
 
 pytestmark = pytest.mark.gpu

@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 from speculative_decoding_tree_build_gb300.build import build
 from speculative_decoding_tree_build_gb300.step import DeviceBatch
 

@@ -12,7 +12,7 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 import bench
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 
 
 def _free_port():

@@ -8,7 +8,7 @@ import math
 import numpy as np
 import pytest
 
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 
 
 def _is_topological(parents):
