@@ -24,7 +24,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kTvNoAllocScrat
 
 // Device address of g_noalloc_scratch per device, looked up on the first call
 // made with that device current. Host code cannot use the array's name as a
-// device pointer: in host code it is only a stand-in for the symbol.
+// device pointer: in host code it is only a stand-in for the symbol. Threads
+// making their first call at the same time may both look the address up and
+// store it; they store the same value, so that race is benign.
 static void* g_scratch_addr[kMaxDevices] = {nullptr};
 
 static int scratch_for_current_device(void** out) {

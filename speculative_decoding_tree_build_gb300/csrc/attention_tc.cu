@@ -18,16 +18,19 @@
 //     page so every row a tile reads is finite.
 //  2. attn_tc_kernel: keys are cache slots [0, P + N); slots >= P are tested
 //     against the node's ancestor bit row. One CTA per SM, warp-specialised:
-//       warp 0      TMA producer: Q tiles, then K and V 16-row pages (4-D
-//                   tensor maps over the paged pools, 128-byte swizzle)
+//       warps 0, 3  TMA producers: warp 0 the Q tiles and per 128-key step
+//                   the K pages, warp 3 the V pages (4-D tensor maps over the
+//                   paged pools, 128-byte swizzle), each with its own barrier
+//       warp 1      MMA issuer for both 128-row M tiles: S = Q K^T (A, B in
+//                   shared memory, N = 128 keys) and O += P V (P read from
+//                   Tensor Memory), fp32 accumulators. The issue order
+//                   S0(j), PV1(j-1), S1(j), PV0(j) makes the tensor core
+//                   alternate between the tiles, so each tile's softmax runs
+//                   while the tensor core works on the other tile; a
+//                   one-tile unit alternates between both score buffers.
 //       warp 2      prefetches the first prompt K/V pages into L2 while the
 //                   pre-pass finishes, then idles (it keeps the softmax
 //                   warps on their lane quarters)
-//       warps 1, 3  MMA issuers, one per 128-row M tile: S = Q K^T (A, B in
-//                   shared memory) and O += P V (P read from Tensor Memory),
-//                   fp32 accumulators. Keys move in 64-key steps and each M
-//                   tile has two 64-column score buffers, so the tensor core
-//                   computes S(j + 1) while the softmax works on S(j).
 //       warps 4-11  two 128-thread softmax groups (one per M tile), one
 //                   Tensor Memory lane (= one query row) per thread.
 //     Query rows of a unit are (node, query head in the GQA group), node
@@ -50,11 +53,8 @@
 
 namespace tv {
 
-constexpr int kTcBN = 128;          // keys per work-plan tile
-constexpr int kTcBK = 64;           // keys per pipeline step (S buffer width, K/V stage)
-constexpr int kTcStages = 4;        // K/V pipeline depth, in steps
+constexpr int kTcBN = 128;          // keys per work-plan tile = per pipeline step (S width)
 constexpr int kTcThreads = 384;     // 12 warps
-constexpr int kExpFmaEvery = 0;     // one exponential pair in this many on the FMA pipe (0: none)
 constexpr int kTcMaxBatch = 4096;
 constexpr int kRopeNodes = 1;       // nodes per pre-pass CTA
 constexpr int kRopeBatch = 4;       // loads in flight per pre-pass thread
@@ -432,67 +432,73 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 2^x on the FMA pipe, for a share of the softmax exponentials so that the
-// MUFU unit is not the only one working. Cody-Waite style reduction
-// x = j + f with j = rint(x) (adding 1.5 * 2^23 rounds x to an integer kept in
-// the low mantissa bits), 2^f for f in [-1/2, 1/2] by a cubic fitted for
-// minimax relative error (Lawson's reweighted least squares; 7.5e-5 at most,
-// far below the bf16 rounding P gets next), and 2^j added to the exponent
-// field. x is clamped at -125 so the exponent stays normal; 2^-125 vanishes
-// in every sum it enters (a fully masked row is discarded by its max).
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float q = fmaf(fmaf(fmaf(5.517166853e-02f, f, 2.426111251e-01f), f, 6.932609677e-01f), f,
-                       9.999280572e-01f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Shared memory and Tensor Memory plan of the attention CTA.
+//  smem: Q of the two M tiles ([tile][64-column half][128 rows x 128 B]),
+//        then kStages K stages and kStages V stages ([half][128 keys x 128 B]
+//        each), all in the 128-byte-swizzled layout TMA writes and the
+//        tensor core reads.
+//  TMEM: S0 = columns [0, 128), S1 = [128, 256) (fp32 scores of one 128-key
+//        step; the softmax writes P as bf16 pairs into the first 64 columns
+//        of the same buffer), O0 and O1 from column 256 (D columns each).
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;                            // 64-column halves of a row
   static constexpr uint32_t kQHalfBytes = 128 * 128;                // Q: 128 rows x 128 B
   static constexpr uint32_t kQBytes = 2 * kHalves * kQHalfBytes;    // two M tiles
-  static constexpr uint32_t kKvHalfBytes = kTcBK * 128;             // K/V stage: 64 keys x 128 B
-  static constexpr uint32_t kStageBytes = kHalves * kKvHalfBytes;   // one K or V stage
-  static constexpr uint32_t kSmem = kQBytes + 2 * kTcStages * kStageBytes;
+  static constexpr uint32_t kHalfBytes = kTcBN * 128;               // K or V: 128 keys x 128 B
+  static constexpr uint32_t kStageBytes = kHalves * kHalfBytes;     // one K or one V stage
+  static constexpr int kStages = D == 128 ? 2 : 4;                  // 128 KB of K/V either way
+  static constexpr uint32_t kSmem = kQBytes + 2 * kStages * kStageBytes;
+  static constexpr uint32_t kOCol = 256;
 };
 
-// Arrival counts: the *_empty barriers take one arrival per MMA issuer (a
-// commit from an issuer with live rows, a plain arrive from one without);
-// p_ready and o_free one per softmax warp of the tile. s_ready / p_ready are
-// per (M tile, score buffer), so each has at most one phase outstanding.
-// kv_empty[s] completing also tells a softmax warp that both tiles' PV of
-// that step (the last MMAs to add to O before the next step) are done.
+constexpr int kTcMaxStages = 4;
+
+// Arrival counts: K and V stages are filled by the producer (one
+// arrive.expect_tx plus the copies' bytes) and released by one tcgen05
+// commit of the MMA issuer (k_empty once the step's S MMAs are done, v_empty
+// once its PV MMAs are done); q_empty, s_full, o_done and pv_done are
+// commits as well; p_full and o_free take one arrival per softmax warp of
+// the group.
 struct TcBars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-  uint64_t s_ready[2][2], p_ready[2][2], o_done[2], o_free[2], drain[2];
+  uint64_t k_full[kTcMaxStages], k_empty[kTcMaxStages];
+  uint64_t v_full[kTcMaxStages], v_empty[kTcMaxStages];
+  uint64_t s_full[3], p_full[3], o_done[2], o_free[2];
+  uint64_t pv_done, drain;
 };
 
-// 64-key steps of a segment (the last one may be partial)
+// Score / P barrier of (role t, score buffer b). Each has one producer and
+// one consumer that sees every phase in order: a parity wait cannot tell a
+// phase that is one ahead from one behind, so no role may skip phases of a
+// barrier another role drives. Index 0: buffer 0 (tile 0, or the even steps
+// of a one-tile segment); 1: buffer 1 in a one-tile segment (softmax group
+// 0); 2: buffer 1 as tile 1's scores (softmax group 1).
+__device__ __forceinline__ int sp_bar(int t, int b) { return t == 1 ? 2 : b; }
+
+// 128-key steps of a segment (the last one may be partial)
 __device__ __forceinline__ int tc_steps(const TcSeg& g) {
   const long long end = static_cast<long long>(g.plen) + g.n;
   const long long hi = min(end, static_cast<long long>(g.tile1) * kTcBN);
-  return static_cast<int>((hi - static_cast<long long>(g.tile0) * kTcBN + kTcBK - 1) / kTcBK);
+  return static_cast<int>((hi - static_cast<long long>(g.tile0) * kTcBN + kTcBN - 1) / kTcBN);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
+  constexpr int kStages = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::kQBytes;
-  uint8_t* sV = sK + kTcStages * C::kStageBytes;
-  int* s_pre = reinterpret_cast<int*>(sV + kTcStages * C::kStageBytes);
+  uint8_t* sV = sK + kStages * C::kStageBytes;
+  int* s_pre = reinterpret_cast<int*>(sV + kStages * C::kStageBytes);
   __shared__ TcBars bars;
   __shared__ int s_tmp[kTcThreads];
   __shared__ uint32_t s_tmem;
@@ -504,20 +510,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     s_abort = 0;
     s_last.valid = false;
     mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 2);
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 2);
+    mbar_init(&bars.q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
-    for (int m = 0; m < 2; ++m) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars.s_ready[m][b], 1);
-        mbar_init(&bars.p_ready[m][b], 4);
-      }
-      mbar_init(&bars.o_done[m], 1);
-      mbar_init(&bars.o_free[m], 4);
-      mbar_init(&bars.drain[m], 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 4);
     }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.o_done[t], 1);
+      mbar_init(&bars.o_free[t], 4);
+    }
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -546,13 +555,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const TcSeg g = tc_segment(p, s_pre, cs, cs, ce, false);
     if (g.valid) {
       const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
-      const int nh = min(tc_steps(g), kTcStages);
+      const int nh = min(tc_steps(g), kStages);
       for (int j = 0; j < nh; ++j) {
-        const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
+        const long long k0 = static_cast<long long>(g.tile0 + j) * kTcBN;
         // stop at the tree's slots, and within the request's table row (an
         // oversized prompt is flagged only by the pre-pass)
-        if (k0 + kTcBK > g.plen || (k0 + kTcBK) / TV_BLOCK_SIZE > p.max_blocks) break;
-        if (lane < kTcBK / TV_BLOCK_SIZE) {
+        if (k0 + kTcBN > g.plen || (k0 + kTcBN) / TV_BLOCK_SIZE > p.max_blocks) break;
+        if (lane < kTcBN / TV_BLOCK_SIZE) {
           const int blk = __ldg(trow + k0 / TV_BLOCK_SIZE + lane);
           if (blk >= 0 && blk < p.num_blocks) {
 #pragma unroll
@@ -570,265 +579,342 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const uint32_t tbase = s_tmem;
   volatile int* abort = &s_abort;
 
-  if (warp == 0) {
-    // ================================================= TMA producer
-    // Streams Q per segment and K + V per 64-key step (four 16-row pages of
-    // each) into one stage with one barrier: the issuer then waits once per
-    // step, and the stage is free once both tiles' PV MMAs (the last readers)
-    // finished. The whole warp runs the loop: lane j fetches page j's
-    // block-table entry and issues that page's copies.
-    uint32_t hc = 0, qs = 0;
+  if (warp == 0 || warp == 3) {
+    // ================================================= TMA producers
+    // Warp 0 streams Q per segment and the K pages of every 128-key step
+    // (eight 16-row pages, two 64-column boxes each) into K stages; warp 3
+    // streams the V pages into V stages. K and V have their own barriers, so
+    // the S MMAs of a step start as soon as its keys have landed, and a K
+    // stage is refilled as soon as the step's S MMAs read it, while its V is
+    // still in use. In each warp lane l issues box l (page l / halves,
+    // 64-column half l % halves) after fetching that page's block-table entry.
+    const bool kw = warp == 0;
+    uint64_t* full = kw ? bars.k_full : bars.v_full;
+    uint64_t* empty = kw ? bars.k_empty : bars.v_empty;
+    const CUtensorMap* map = kw ? &p.kmap : &p.vmap;
+    uint8_t* stage0 = kw ? sK : sV;
+    uint32_t hc = 0, qs = 0;           // steps whose copies were issued; segments
     bool ok = true;
     for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
          g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
-      if (lane == 0) s_last = g;
+      if (kw && lane == 0) s_last = g;
       if (g.skip) continue;
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
-      if (!ok) break;
-      ++qs;
-      if (lane == 0) {
-        // one box of npq nodes x G heads (<= 32 rows) per quarter and half;
-        // quarters without nodes are not loaded
-        const RowSplit rs = row_split(g.nodes, g.mt);
-        const uint32_t qbox = 64u * 2u * G * npq;
-        const int nq = min(4 * g.mt, g.nodes);
-        mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * nq);
-        for (int j = 0; j < nq; ++j)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_4d(sQ + ((j >> 2) * C::kHalves + h) * C::kQHalfBytes + (j & 3) * 4096, &p.qmap,
-                        h * 64, 0, g.kvh, g.t0 + g.node0 + quarter_first(rs, j), &bars.q_full);
+      if (kw) {
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
+        if (!ok) break;
+        ++qs;
+        if (lane == 0) {
+          // one box of npq nodes x G heads (<= 32 rows) per quarter and half;
+          // quarters without nodes are not loaded
+          const RowSplit rs = row_split(g.nodes, g.mt);
+          const uint32_t qbox = 64u * 2u * G * npq;
+          const int nq = min(4 * g.mt, g.nodes);
+          mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * nq);
+          for (int j = 0; j < nq; ++j)
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_4d(sQ + ((j >> 2) * C::kHalves + h) * C::kQHalfBytes + (j & 3) * 4096, &p.qmap,
+                          h * 64, 0, g.kvh, g.t0 + g.node0 + quarter_first(rs, j), &bars.q_full);
+        }
       }
       const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
       const long long end = static_cast<long long>(g.plen) + g.n;
       const int nh = tc_steps(g);
-      for (int j = 0; j < nh; ++j, ++hc) {
-        const int s = hc % kTcStages;
-        const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
-        const int np = static_cast<int>((min(end, k0 + kTcBK) - k0 + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
-        const int blk = lane < np ? __ldg(trow + k0 / TV_BLOCK_SIZE + lane) : 0;
-        ok = __shfl_sync(0xffffffffu,
-                         lane == 0 ? mbar_wait(&bars.kv_empty[s], ((hc / kTcStages) & 1) ^ 1, abort) : false, 0);
+      for (int j = 0; j < nh; ++j) {
+        const int s = hc % kStages;
+        const uint32_t ph = ((hc / kStages) & 1) ^ 1;
+        const long long k0 = static_cast<long long>(g.tile0 + j) * kTcBN;
+        const int np = static_cast<int>((min(end, k0 + kTcBN) - k0 + TV_BLOCK_SIZE - 1) / TV_BLOCK_SIZE);
+        const int pg = lane / C::kHalves, h = lane % C::kHalves;
+        const bool mine = pg < np;
+        const int blk = mine ? __ldg(trow + k0 / TV_BLOCK_SIZE + pg) : 0;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&empty[s], ph, abort) : false, 0);
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars.kv_full[s], np * C::kHalves * 2u * 2048u);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], np * C::kHalves * 2048u);
         __syncwarp();
-        if (lane < np) {
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            tma_load_4d(sK + s * C::kStageBytes + h * C::kKvHalfBytes + lane * 2048, &p.kmap, h * 64, 0,
-                        g.kvh, blk, &bars.kv_full[s]);
-            tma_load_4d(sV + s * C::kStageBytes + h * C::kKvHalfBytes + lane * 2048, &p.vmap, h * 64, 0,
-                        g.kvh, blk, &bars.kv_full[s]);
-          }
-        }
+        if (mine)
+          tma_load_4d(stage0 + s * C::kStageBytes + h * C::kHalfBytes + pg * 2048, map, h * 64, 0, g.kvh,
+                      blk, &full[s]);
+        ++hc;
       }
     }
-    // never leave copies in flight: wait for the stages this warp filled
-    for (uint32_t k = (hc > kTcStages ? hc - kTcStages : 0); lane == 0 && k < hc; ++k) {
+    // never leave copies in flight: wait for the last kStages stages this
+    // warp filled (and the last Q)
+    for (uint32_t k = (hc > kStages ? hc - kStages : 0); lane == 0 && k < hc; ++k) {
       volatile int no_abort = 0;
-      mbar_wait(&bars.kv_full[k % kTcStages], (k / kTcStages) & 1, &no_abort);
+      mbar_wait(&full[k % kStages], (k / kStages) & 1, &no_abort);
     }
-  } else if (warp == 1 || warp == 3) {
-    // ================================================= MMA issuers
-    // Warp 1 issues every MMA of M tile 0, warp 3 of M tile 1 (a thread needs
-    // about 60 cycles per tcgen05.mma; two issuers keep one tile's waits off
-    // the other's path). Each tile has two 64-key score buffers, so S(j + 1)
-    // is computed while the softmax works on S(j); the order per tile is
+    if (kw && lane == 0 && qs > 0) {
+      volatile int no_abort = 0;
+      mbar_wait(&bars.q_full, (qs - 1) & 1, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    // One thread issues every MMA, so the tensor core alternates between the
+    // two M tiles: per 128-key step j of a two-tile segment
+    //   S0(j) = Q0 K(j)^T,  O1 += P1(j-1) V(j-1),  S1(j) = Q1 K(j)^T,  O0 += P0(j) V(j)
+    // and while the tensor core runs PV1 and S1, the softmax of tile 0 turns
+    // S0 into P0, and vice versa. MMAs of one thread execute in order, so
+    // S_t(j+1) may overwrite the columns P_t(j) occupies once PV_t(j) is
+    // issued, and the commit that signals S_t(j) also covers PV_t(j-1): the
+    // softmax may then rescale O_t in place. A one-tile segment alternates
+    // between both score buffers instead,
     //   S(0), S(1), PV(0), S(2), PV(1), S(3), ...
-    // MMAs of one thread run in order, which is what lets S(j + 2) reuse the
-    // buffer P(j) occupies once PV(j) is issued. An issuer without rows in a
-    // segment still takes part in the stage hand-off with plain arrivals.
+    // so S(j+1) is computed while the softmax works on S(j); there the PV
+    // completions are signalled separately for the softmax's rare O rescale.
     if (lane == 0) {
-      const int m = warp >> 1;
-      constexpr uint32_t idS = idesc_bf16_f32(128, kTcBK, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, kTcBN, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
       // descriptors built once; each K step only adds a compile-time offset
       // (the start-address field is the low 14 bits, in 16-byte units, and
       // shared-memory addresses stay below 256 KB, so it never carries out)
-      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ) + m * C::kHalves * C::kQHalfBytes, 16, 1024);
+      const uint64_t dQ0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dQ1 = smem_desc_sw128(smem_u32(sQ) + C::kHalves * C::kQHalfBytes, 16, 1024);
       const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::kKvHalfBytes, 1024);
-      const uint32_t tO = tbase + m * 128;
-      uint32_t hc = 0, hb = 0, qs = 0, pcnt[2] = {0, 0}, of = 0;
-      bool used = false, ok = true;
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::kHalfBytes, 1024);
+      uint32_t hc = 0, qs = 0, pc[3] = {0, 0, 0}, of[2] = {0, 0};   // pc: P phases seen per barrier
+      bool used[2] = {false, false}, ok = true;
+      // S = Q_t K(stage s)^T into score buffer b (its barrier: role t)
+      auto issue_s = [&](int t, int s, int b) {
+        const uint64_t dq = t == 0 ? dQ0 : dQ1;
+        const uint64_t bk = dK + s * (C::kStageBytes / 16);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)                        // 32 bytes per K step
+          mma_ss(tbase + b * 128, dq + (k / 4) * (C::kQHalfBytes / 16) + (k % 4) * 2,
+                 bk + (k / 4) * (C::kHalfBytes / 16) + (k % 4) * 2, idS, k > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full[sp_bar(t, b)]);
+      };
+      // waits for P_t in buffer b and, before the tile's first PV of a
+      // segment, for the epilogue to have read O_t out; then O_t += P V(stage
+      // s) for step j (16-key chunks past the request's last key are not
+      // issued: their V rows were never loaded)
+      auto issue_pv = [&](int t, int s, int b, int j, const TcSeg& g) -> bool {
+        const int bi = sp_bar(t, b);
+        if (!mbar_wait(&bars.p_full[bi], pc[bi] & 1, abort)) return false;
+        ++pc[bi];
+        if (j == 0 && used[t]) {
+          if (!mbar_wait(&bars.o_free[t], of[t] & 1, abort)) return false;
+          ++of[t];
+        }
+        tc_fence_after();
+        const long long end = static_cast<long long>(g.plen) + g.n;
+        const long long k0 = static_cast<long long>(g.tile0 + j) * kTcBN;
+        const int kch = static_cast<int>((min(end, k0 + kTcBN) - k0 + 15) / 16);
+        const uint32_t tO = tbase + C::kOCol + t * D;
+        const uint64_t bv = dV + s * (C::kStageBytes / 16);
+        if (kch == kTcBN / 16) {
+#pragma unroll
+          for (int k = 0; k < kTcBN / 16; ++k)
+            mma_ts(tO, tbase + b * 128 + k * 8, bv + k * (2048 / 16), idO, (j > 0 || k > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kTcBN / 16; ++k)
+            if (k < kch)
+              mma_ts(tO, tbase + b * 128 + k * 8, bv + k * (2048 / 16), idO, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        return true;
+      };
       for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
            g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
         if (g.skip) continue;
         if (!(ok = mbar_wait(&bars.q_full, qs & 1, abort))) break;
         ++qs;
+        tc_fence_after();
         const int nh = tc_steps(g);
-        if (m >= g.mt) {
-          // no rows here: pace the hand-off on the stages' fills, then release them
+        if (g.mt == 2) {
           for (int j = 0; j < nh && ok; ++j) {
             const uint32_t h = hc + j;
-            if (!(ok = mbar_wait(&bars.kv_full[h % kTcStages], (h / kTcStages) & 1, abort))) break;
-            mbar_arrive(&bars.kv_empty[h % kTcStages]);
-            if (j == nh - 1) mbar_arrive(&bars.q_empty);
+            const int s = h % kStages;
+            const uint32_t ph = (h / kStages) & 1;
+            if (!(ok = mbar_wait(&bars.k_full[s], ph, abort))) break;
+            tc_fence_after();
+            issue_s(0, s, 0);
+            if (j > 0) {
+              const int sp = (h - 1) % kStages;
+              if (!(ok = issue_pv(1, sp, 1, j - 1, g))) break;
+              mma_commit(&bars.v_empty[sp]);                  // both tiles' PV of step j-1 issued
+            }
+            issue_s(1, s, 1);
+            mma_commit(&bars.k_empty[s]);
+            if (j == nh - 1) mma_commit(&bars.q_empty);       // the segment's last S MMAs
+            if (!(ok = mbar_wait(&bars.v_full[s], ph, abort))) break;
+            if (!(ok = issue_pv(0, s, 0, j, g))) break;
+            if (j == nh - 1) mma_commit(&bars.o_done[0]);
           }
-          hc += nh;
-          continue;
-        }
-        tc_fence_after();
-        const long long end = static_cast<long long>(g.plen) + g.n;
-        auto issue_s = [&](int j) -> bool {
-          const uint32_t h = hc + j;
-          const int s = h % kTcStages;
-          if (!mbar_wait(&bars.kv_full[s], (h / kTcStages) & 1, abort)) return false;
-          tc_fence_after();
-          const int b = (hb + j) & 1;
-          const uint32_t tS = tbase + 256 + m * 128 + b * 64;
-          const uint64_t bk = dK + s * (C::kStageBytes / 16);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)                      // 32 bytes per K step
-            mma_ss(tS, dQ + (k / 4) * (C::kQHalfBytes / 16) + (k % 4) * 2,
-                   bk + (k / 4) * (C::kKvHalfBytes / 16) + (k % 4) * 2, idS, k > 0 ? 1u : 0u);
-          mma_commit(&bars.s_ready[m][b]);
-          if (j == nh - 1) mma_commit(&bars.q_empty);           // the last S of the segment
-          return true;
-        };
-        ok = issue_s(0);
-        if (ok && nh > 1) ok = issue_s(1);
-        for (int j = 0; j < nh && ok; ++j) {
-          const uint32_t h = hc + j;
-          const int s = h % kTcStages;
-          const int b = (hb + j) & 1;
-          if (!(ok = mbar_wait(&bars.p_ready[m][b], pcnt[b] & 1, abort))) break;
-          ++pcnt[b];
-          if (j == 0 && used) {
-            if (!(ok = mbar_wait(&bars.o_free[m], of & 1, abort))) break;
-            ++of;
+          if (ok) {
+            const int sl = (hc + nh - 1) % kStages;
+            if ((ok = issue_pv(1, sl, 1, nh - 1, g))) {
+              mma_commit(&bars.v_empty[sl]);
+              mma_commit(&bars.o_done[1]);
+            }
           }
-          tc_fence_after();                                     // K + V of the step landed before S(j)
-          const long long k0 = static_cast<long long>(g.tile0) * kTcBN + static_cast<long long>(j) * kTcBK;
-          const int kch = static_cast<int>((min(end, k0 + kTcBK) - k0 + 15) / 16);
-          const uint32_t tP = tbase + 256 + m * 128 + b * 64;
-          const uint64_t bv = dV + s * (C::kStageBytes / 16);
-#pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k)                  // 16 keys (2048 B of V) per step
-            if (k < kch) mma_ts(tO, tP + k * 8, bv + k * (2048 / 16), idO, (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bars.kv_empty[s]);
-          if (j == nh - 1) mma_commit(&bars.o_done[m]);
-          if (j + 2 < nh) ok = issue_s(j + 2);
+          used[1] = true;
+        } else {
+          auto s_step = [&](int j) -> bool {
+            const uint32_t h = hc + j;
+            const int s = h % kStages;
+            if (!mbar_wait(&bars.k_full[s], (h / kStages) & 1, abort)) return false;
+            tc_fence_after();
+            issue_s(0, s, j & 1);
+            mma_commit(&bars.k_empty[s]);
+            if (j == nh - 1) mma_commit(&bars.q_empty);
+            return true;
+          };
+          ok = s_step(0);
+          if (ok && nh > 1) ok = s_step(1);
+          for (int j = 0; j < nh && ok; ++j) {
+            const uint32_t h = hc + j;
+            const int s = h % kStages;
+            if (!(ok = mbar_wait(&bars.v_full[s], (h / kStages) & 1, abort))) break;
+            if (!(ok = issue_pv(0, s, j & 1, j, g))) break;
+            mma_commit(&bars.v_empty[s]);
+            mma_commit(&bars.pv_done);
+            if (j == nh - 1) mma_commit(&bars.o_done[0]);
+            if (j + 2 < nh) ok = s_step(j + 2);
+          }
         }
-        used = true;
         hc += nh;
-        hb += nh;
+        used[0] = true;
       }
       // drain: every MMA this thread issued completes before Tensor Memory is freed
-      mma_commit(&bars.drain[m]);
+      mma_commit(&bars.drain);
       volatile int no_abort = 0;
-      mbar_wait(&bars.drain[m], 0, &no_abort);
+      mbar_wait(&bars.drain, 0, &no_abort);
     }
   } else if (warp >= 4) {
     // ================================================= softmax groups
     // warps 4-7 serve M tile 0, warps 8-11 M tile 1; warp w owns Tensor
-    // Memory lanes 32 * (w % 4) .. +31, one query row per thread.
-    const int m = (warp - 4) >> 2;
+    // Memory lanes 32 * (w % 4) .. +31, one query row per thread. A step's
+    // 128 scores are taken in two halves of 64; P of each half goes as bf16
+    // pairs into the buffer's columns already read. In a one-tile segment
+    // group 0 takes every step, from both score buffers in turn.
+    const int t = (warp - 4) >> 2;
     const int qd = warp & 3;
-    const int j4 = 4 * m + qd;                         // quarter of the unit's rows
+    const int j4 = 4 * t + qd;                         // quarter of the unit's rows
     const uint32_t lane_addr = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tO = tbase + m * 128 + lane_addr;
-    uint32_t hb = 0, hcs = 0, scnt[2] = {0, 0}, oc = 0;
+    const uint32_t tO = tbase + C::kOCol + t * D + lane_addr;
+    const uint64_t scale2 = f32x2_pack(p.scale_log2, p.scale_log2);
+    uint32_t sc[2] = {0, 0}, oc = 0, pvc = 0;        // sc: score phases seen per buffer
     bool ok = true;
     for (TcSeg g = tc_segment(p, s_pre, cs, cs, ce); ok && g.valid;
          g = tc_segment(p, s_pre, g.t_next, cs, ce)) {
       if (g.skip) continue;
       const int nh = tc_steps(g);
-      if (m >= g.mt) {
-        hcs += nh;
-        continue;
-      }
+      const bool one = g.mt == 1;
+      if (one && t == 1) continue;           // group 0 takes both buffers here
       const RowSplit rs = row_split(g.nodes, g.mt);
       const int cnt = quarter_count(rs, j4);
       const bool warp_live = cnt > 0;                  // uniform over the warp
       const bool row_valid = lane < G * cnt;
       const int nd = g.node0 + quarter_first(rs, j4) + (row_valid ? lane / G : 0);   // node of this row
-      float m_ref = -INFINITY, l_a = 0.f, l_b = 0.f;
+      float m_ref = -INFINITY;
+      uint64_t l2 = f32x2_pack(0.f, 0.f);              // running row sum, two partial sums
       const uint32_t* mrow = p.mask + static_cast<size_t>(g.t0 + nd) * p.words;
       for (int j = 0; j < nh && ok; ++j) {
-        const int b = (hb + j) & 1;
-        if (!(ok = mbar_wait(&bars.s_ready[m][b], scnt[b] & 1, abort))) break;
-        ++scnt[b];
+        const int b = one ? (j & 1) : t;
+        if (!(ok = mbar_wait(&bars.s_full[sp_bar(t, b)], sc[b] & 1, abort))) break;
+        ++sc[b];
         tc_fence_after();
         if (warp_live) {
-          const uint32_t tS = tbase + 256 + m * 128 + b * 64 + lane_addr;
-          const int k0 = g.tile0 * kTcBN + j * kTcBK;
-          uint32_t a[kTcBK];
-          tmem_ld32(tS, a);
-          tmem_ld32(tS + 32, a + 32);
-          tmem_ld_wait();
-          if (k0 + kTcBK > g.plen) {                   // the step reaches past the prompt: mask it
-#pragma unroll
-            for (int c = 0; c < kTcBK / 32; ++c) {
-              const uint32_t vis = row_valid ? visible_bits(mrow, p.words, g.plen, g.n, k0 + c * 32) : 0u;
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (!((vis >> e) & 1u)) a[c * 32 + e] = 0xFF800000u;   // -inf
-            }
-          }
-          float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < kTcBK; e += 8) {
-            x0 = fmax3(x0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-            x1 = fmax3(x1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-            x2 = fmax3(x2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
-            x3 = fmax3(x3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
-          }
-          const float mxs = fmax3(x0, x1, fmaxf(x2, x3)) * p.scale_log2;
-          // Lazy rescale: keep the reference max until a score exceeds it by
-          // 2^8; p stays <= 2^8 and O, l share the same reference. O is only
-          // rescaled once PV(j - 1), the last MMA that adds to it, is done.
-          if (mxs > m_ref + 8.f) {
-            if (m_ref != -INFINITY) {
-              const float alpha = fast_exp2(m_ref - mxs);
-              l_a *= alpha;
-              l_b *= alpha;
-              const uint32_t hp = hcs + j - 1;                  // the step whose PVs last added to O
-              ok = mbar_wait(&bars.kv_empty[hp % kTcStages], (hp / kTcStages) & 1, abort);
-              tc_fence_after();
+          const uint32_t tS = tbase + b * 128 + lane_addr;
+          const int k0 = (g.tile0 + j) * kTcBN;
 #pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait();
+          for (int hf = 0; hf < 2; ++hf) {
+            const int kh = k0 + hf * 64;
+            uint32_t a[64];
+            tmem_ld32(tS + hf * 64, a);
+            tmem_ld32(tS + hf * 64 + 32, a + 32);
+            tmem_ld_wait();
+            if (kh + 64 > g.plen) {                    // the half reaches past the prompt: mask it
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                tmem_st32(tO + c * 32, o);
+              for (int c = 0; c < 2; ++c) {
+                const uint32_t vis = row_valid ? visible_bits(mrow, p.words, g.plen, g.n, kh + c * 32) : 0u;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (!((vis >> e) & 1u)) a[c * 32 + e] = 0xFF800000u;   // -inf
               }
             }
-            m_ref = mxs;
-          }
-          const float base = m_ref == -INFINITY ? 0.f : m_ref;
-          // p = 2^(s * scale * log2(e) - base) as bf16 into the buffer's first 32 columns
+            float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kTcBK / 32; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float y0 = fmaf(__uint_as_float(a[c * 32 + 2 * e]), p.scale_log2, -base);
-              const float y1 = fmaf(__uint_as_float(a[c * 32 + 2 * e + 1]), p.scale_log2, -base);
-              // one pair in kExpFmaEvery on the FMA pipe, the rest on MUFU
-              const bool on_fma = kExpFmaEvery > 0 && e % kExpFmaEvery == kExpFmaEvery - 1;
-              const float p0 = on_fma ? exp2_fma(y0) : fast_exp2(y0);
-              const float p1 = on_fma ? exp2_fma(y1) : fast_exp2(y1);
-              l_a += p0;
-              l_b += p1;
-              pk[e] = pack_bf16x2(p0, p1);
+            for (int e = 0; e < 64; e += 8) {
+              x0 = fmax3(x0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+              x1 = fmax3(x1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+              x2 = fmax3(x2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+              x3 = fmax3(x3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
             }
-            tmem_st16(tS + c * 16, pk);
+            const float mxs = fmax3(x0, x1, fmaxf(x2, x3)) * p.scale_log2;
+            // Lazy rescale: the reference max moves only when a score exceeds
+            // it by 2^8, so p stays <= 2^8 and O, l share one reference. A
+            // move rescales O (once its previous step's PV is complete) and,
+            // in the second half, the P already written for the first half.
+            // The Tensor Memory accesses are warp-wide, so a warp rescales
+            // when any of its rows moved (alpha = 1 for the others).
+            float alpha = 1.f;
+            if (mxs > m_ref + 8.f) {
+              if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - mxs);
+              m_ref = mxs;
+            }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+              l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
+              if (j > 0) {
+                if (one) {                             // PV(j - 1) may still be running
+                  volatile int* ab = abort;
+                  ok = mbar_wait(&bars.pv_done, (pvc + j - 1) & 1, ab);
+                  tc_fence_after();
+                }
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                  uint32_t o[32];
+                  tmem_ld32(tO + c * 32, o);
+                  tmem_ld_wait();
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                  tmem_st32(tO + c * 32, o);
+                }
+              }
+              if (hf == 1) {
+                uint32_t o[32];
+                tmem_st_wait();                        // the first half's P is in place
+                tmem_ld32(tS, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = pack_bf16x2(bf16_lo(o[e]) * alpha, bf16_hi(o[e]) * alpha);
+                tmem_st32(tS, o);
+              }
+            }
+            const float base = m_ref == -INFINITY ? 0.f : m_ref;
+            const uint64_t nb2 = f32x2_pack(-base, -base);
+            // p = 2^(s * scale * log2(e) - base), two at a time, as bf16 pairs
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float y0, y1;
+                f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(a[c * 32 + 2 * e]),
+                                                  __uint_as_float(a[c * 32 + 2 * e + 1])),
+                                       scale2, nb2), y0, y1);
+                const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                const uint64_t pp = f32x2_pack(p0, p1);
+                l2 = f32x2_add(l2, pp);
+                pk[e] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(tS + hf * 32 + c * 16, pk);
+            }
           }
           tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.p_ready[m][b]);
+        if (lane == 0) mbar_arrive(&bars.p_full[sp_bar(t, b)]);
       }
-      hb += nh;
-      hcs += nh;
-      if (ok && (ok = mbar_wait(&bars.o_done[m], oc & 1, abort))) {
+      if (one) pvc += nh;
+      if (ok && (ok = mbar_wait(&bars.o_done[t], oc & 1, abort))) {
         ++oc;
         tc_fence_after();
         if (warp_live) {
-          const float l_sum = l_a + l_b;
+          float la, lb;
+          f32x2_unpack(l2, la, lb);
+          const float l_sum = la + lb;
           const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
           if (g.whole) {
             const int h = g.kvh * G + lane % G;
@@ -881,7 +967,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.o_free[m]);
+        if (lane == 0) mbar_arrive(&bars.o_free[t]);
       }
       if (!ok) break;
     }

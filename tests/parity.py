@@ -113,6 +113,7 @@ def run_gpu(w, calls=("build", "attn", "accept", "commit"), db=None):
 def check_tree_outputs(db, ref, w):
     cu = w["cu_nodes"]
     st = db.status.cpu().numpy()
+    assert not np.any(st & 32), "a bounded device wait expired (TV_ST_TIMEOUT)"
     assert np.array_equal(st & 7, ref["status"] & 7)
     for b in range(w["batch"]):
         if ref["status"][b] & 7:

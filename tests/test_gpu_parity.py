@@ -165,7 +165,7 @@ def _star(n):
 @pytest.mark.parametrize("case", ["empty_prompt", "root_only", "chain_1024", "star_300",
                                   "block_edges", "group16_d64_halfsplit", "tail_g1_16_nodes",
                                   "tail_g16_d64_one_node", "tail_g8_halfsplit", "batch_4096_roots",
-                                  "many_tiny_trees"])
+                                  "many_tiny_trees", "mixed_unit_shapes"])
 def test_attention_edge_cases(case):
     """Degenerate and boundary shapes. The tail_* cases end a KV head's query
     rows with a unit of at most 16 rows after full 256-row units: 16 nodes of
@@ -174,7 +174,11 @@ def test_attention_edge_cases(case):
     and merged. batch_4096_roots is the largest batch the library takes (one
     root node each, prompts of 0-16 tokens: the work plan's prefix over the
     batch at its largest); many_tiny_trees gives every CTA dozens of
-    one-tile units in a row."""
+    one-tile units in a row. mixed_unit_shapes gives every CTA a run of
+    units whose row counts alternate between one and two 128-row tiles (and
+    256-row units followed by short remainders), so the CTA's two MMA
+    issuers and two softmax groups hand the score buffers back and forth
+    between segments."""
     if case == "empty_prompt":
         w = _custom(wl.GEOM_8B, [wl.medusa_tree(np.random.default_rng(1), (4, 3), 100)] * 2, [0, 0])
     elif case == "root_only":
@@ -199,6 +203,12 @@ def test_attention_edge_cases(case):
         rng = np.random.default_rng(12)
         trees = [wl.eagle_tree(rng, 2, 3, int(rng.integers(1, 6)), 1000)[:2] for _ in range(1500)]
         w = _custom(wl.Geometry(8, 2, 128), trees, list(rng.integers(0, 200, 1500)))
+    elif case == "mixed_unit_shapes":
+        rng = np.random.default_rng(13)
+        sizes = [1, 40, 9, 65, 33, 2, 64, 20, 70, 5] * 6
+        trees = [wl.eagle_tree(rng, 0, int(rng.integers(3, 9)), n - 1, 1000, until_count=True)[:2]
+                 if n > 1 else ([-1], [1]) for n in sizes]
+        w = _custom(wl.GEOM_8B, trees, list(rng.integers(100, 700, len(sizes))))
     elif case == "tail_g8_halfsplit":
         rng = np.random.default_rng(5)
         trees = [wl.eagle_tree(rng, 4, 4, 32, 1000)[:2], _star(34), _chain(33)]

@@ -83,6 +83,16 @@ def test_host_validation_rejects_before_launch(lib):
                               None) == -2
     assert L.tv_kv_commit(ctypes.byref(g), 1, P, P, 4, P, None, P, 8, P, P, 10, P, P, P, P,
                           None) == -1
+    # a K+V row of every KV head must fit the commit's 64 KiB staging buffer:
+    # 256 KV heads x 128 x 2 x 2 bytes = 128 KiB does not (refused before any launch)
+    wide = tv.geom(256, 256, 128)
+    assert L.tv_kv_commit(ctypes.byref(wide), 1, P, P, 4, P, P, P, 8, P, P, 10, P, P, P, P,
+                          None) == -2
+    assert L.tv_accept_commit(ctypes.byref(wide), P, P, P, P, P, 1, 41, 4, P, P, P, P, P, P, 8,
+                              P, P, 10, P, P, P, P, None) == -2
+    fits = tv.geom(128, 128, 128)                         # exactly 64 KiB per row
+    assert L.tv_kv_commit(ctypes.byref(fits), 0, None, None, 4, None, None, None, 8, None, None,
+                          10, None, None, None, None, None) == 0
     assert L.tv_kv_commit(ctypes.byref(g), 0, None, None, 4, None, None, None, 8, None, None, 10,
                           None, None, None, None, None) == 0
     # attention
@@ -180,35 +190,6 @@ def test_host_validation_rejects_before_launch(lib):
     assert M(P, P, P, P, 2, 0, 0, 0, P, None) == -3
     assert M(P, P, P, None, 2, 41, 0, 0, P, None) == -1
     assert M(P, P, P, P, 2, 41, 0, 1, P + 2, None) == -5    # float32 out not aligned
-
-
-def test_fma_exp2_cubic_error_bound():
-    """The cubic that can replace MUFU exp2 for a share of the softmax
-    (attention_tc.cu, exp2_fma) stays within 8e-5 relative error of 2^f on
-    [-1/2, 1/2] when evaluated in fp32 Horner form, and the range reduction
-    x = j + f with j = rint(x) reproduces 2^x on the kernel's input range."""
-    import numpy as np
-
-    with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", "attention_tc.cu"),
-              encoding="utf-8") as fh:
-        src = fh.read()
-    body = src[src.index("float exp2_fma(float x)"):]
-    body = body[:body.index("}")]
-    coefs = [float(c) for c in re.findall(r"([0-9]\.[0-9]+e[-+][0-9]+)f", body)]
-    assert len(coefs) == 4                      # c3, c2, c1, c0 in Horner order
-    c3, c2, c1, c0 = (np.float32(c) for c in coefs)
-    f = np.linspace(-0.5, 0.5, 200001).astype(np.float32)
-    q = ((c3 * f + c2) * f + c1) * f + c0
-    rel = np.abs(q.astype(np.float64) / np.exp2(f.astype(np.float64)) - 1.0)
-    assert rel.max() < 8e-5
-    # full path on x in [-125, 8]: round to nearest integer via 1.5 * 2^23, scale by 2^j
-    x = np.linspace(-125.0, 8.0, 100001).astype(np.float32)
-    t = (x + np.float32(12582912.0)).astype(np.float32)
-    ff = (x - (t - np.float32(12582912.0))).astype(np.float32)
-    qq = (((c3 * ff + c2) * ff + c1) * ff + c0).astype(np.float32)
-    bits = qq.view(np.int32) + (t.view(np.int32) << 23)
-    y = bits.view(np.float32).astype(np.float64)
-    assert np.all(np.abs(y / np.exp2(x.astype(np.float64)) - 1.0) < 8e-5)
 
 
 def test_missing_library_fails_loudly(tmp_path):

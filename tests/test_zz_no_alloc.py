@@ -4,8 +4,8 @@ It serves callers that cannot allocate device memory (a plugin that only gets
 a stream and tensors from its host framework, code running while another
 component owns the device memory pool, a loop that must not call cudaMalloc).
 Its scratch lives in a fixed array inside the library, so these tests check
-that it gives the same outputs as the workspace entry point, call after call
-on the shared array, and that oversized work is refused up front.
+that it gives the same outputs as the workspace entry point, bit for bit, call
+after call on the shared array, and that oversized work is refused up front.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -18,11 +18,9 @@ import pytest
 import torch
 
 import speculative_decoding_tree_build_gb300 as tv
-from speculative_decoding_tree_build_gb300 import workloads as wl
+from gen import workloads as wl
 from speculative_decoding_tree_build_gb300.build import build
 from speculative_decoding_tree_build_gb300.step import DeviceBatch
-
-from parity import ATOL, REL_FRO
 
 pytestmark = pytest.mark.gpu
 
@@ -38,12 +36,14 @@ def _noalloc_call(lib, db, out, status):
         torch.cuda.current_stream().cuda_stream)
 
 
-def _close(got, want):
-    g = got.float().cpu().numpy().astype(np.float64)
-    r = want.float().cpu().numpy().astype(np.float64)
-    assert np.all(np.isfinite(g))
-    assert np.max(np.abs(g - r)) <= ATOL
-    assert np.linalg.norm(g - r) / np.linalg.norm(r) <= REL_FRO
+def _same(got, want):
+    """Both entry points run the same kernels with the same work plan, so the
+    outputs must agree bit for bit; any difference would point at scratch
+    records left over from a previous call."""
+    g = got.view(torch.int16).cpu().numpy()
+    r = want.view(torch.int16).cpu().numpy()
+    assert np.array_equal(g, r), f"{int(np.count_nonzero(g != r))} outputs differ"
+    assert np.all(np.isfinite(got.float().cpu().numpy()))
 
 
 @pytest.mark.parametrize("cfg", [2, 5])
@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_point_twice(cfg):
         assert _noalloc_call(lib, db, out, status) == 0
         torch.cuda.synchronize()
         assert int(status.abs().sum()) == 0
-        _close(out, want)
+        _same(out, want)
 
 
 def test_noalloc_rejects_work_larger_than_its_scratch():
@@ -83,3 +83,7 @@ def test_noalloc_rejects_work_larger_than_its_scratch():
         db.v_cache.data_ptr(), db.k_cache.shape[0], out.data_ptr(), db.status.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
     assert rc == -4 and tv.status_string(rc) == "TV_ERR_WORKSPACE"
+    # refused before any launch: nothing was written
+    torch.cuda.synchronize()
+    assert int(out.view(torch.int16).abs().sum()) == 0
+    assert int(db.status.abs().sum()) == 0
