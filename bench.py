@@ -1,11 +1,18 @@
-"""Benchmark of one token-tree verification step on GB300.
+"""Benchmark of the token-tree verification step on GB300.
 
 A step is the whole hot path over one batch: tv_tree_build ->
-tv_tree_attention_verify -> tv_greedy_accept -> tv_kv_commit (plus the
-block-table refill a serving loop's allocator does before the next step).
-The default workload is the Llama-3-8B attention geometry, batch 8, prompt
-lengths U[512, 2048], Medusa 4x3x2 trees (41 nodes incl. root), paged KV
-block 16 with a shuffled block table.
+tv_tree_attention_verify -> tv_accept_commit (greedy accept + KV commit with
+block release), after the block-table refill a serving loop's allocator does.
+
+The headline workload (config 5) is the Llama-3-8B attention geometry, batch
+64 ragged, prompts log-uniform in [4096, 32768], random EAGLE-style trees of
+16-128 nodes (+ root), run as eight evolving steps: each step commits the
+accepted path, releases blocks past the new end, the host allocator hands the
+next tree's slots out of the free list, and the next tree is verified at
+P + 1 + a. The eight steps are generated once, then replayed in order; the
+timed steps cycle through them. Configs 2, 3 and 4 are measured as one
+verification step each (`sub_workloads`). ``--config C`` makes config C the
+headline instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
 
@@ -35,17 +42,25 @@ sys.path.insert(0, ROOT)
 METRIC = "tree-verify tokens/s at 1 GB300; attention HBM GB/s & % roofline per step"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
+MULTISTEP = 8                 # config 5: verification steps of one request cycle
+SUB_CONFIGS = (2, 3, 4)
 ATTN_SOURCES = ("attention_tc.cu", "tv_sm100.cuh", "tv_common.cuh")
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=80,
+                    help="timed verification steps (config 5: the eight evolving steps in turn)")
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--config", type=int, default=5)
+    ap.add_argument("--attn-iters", type=int, default=30,
+                    help="timed launches of each step's attention call")
+    ap.add_argument("--sub-iters", type=int, default=200,
+                    help="timed steps of each of the other workloads (configs 2-4)")
+    ap.add_argument("--no-sub", action="store_true", help="skip the other workloads")
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sampling-steps", type=int, default=200,
@@ -530,14 +545,15 @@ def _sub_workload(w, b):
     return sub
 
 
-def cpu_baseline(w, seconds):
+def cpu_baseline(w, seconds, node_limit=None):
     """Time the oracle (as it stands) on the host cores: one spawn worker per
-    core, single-threaded BLAS, each worker verifying whole requests."""
+    core, single-threaded BLAS, each worker verifying requests (all query
+    heads of the first ``node_limit`` nodes of each, or every node)."""
     cores = os.cpu_count() or 1
     ctx = mp.get_context("spawn")
     batch = w["batch"]
     # calibrate on one request
-    n0, t_one = _oracle_worker((w, [0], None))
+    n0, t_one = _oracle_worker((w, [0], node_limit))
     per_req = max(t_one, 1e-3)
     reqs_total = max(1, int(seconds * cores / per_req))
     order = [i % batch for i in range(reqs_total)]
@@ -545,13 +561,14 @@ def cpu_baseline(w, seconds):
     chunks = [c for c in chunks if c]
     t0 = time.perf_counter()
     with ctx.Pool(len(chunks)) as pool:
-        res = pool.map(_oracle_worker, [(w, c, None) for c in chunks])
+        res = pool.map(_oracle_worker, [(w, c, node_limit) for c in chunks])
     wall = time.perf_counter() - t0
     nodes = sum(r[0] for r in res)
+    what = "every node" if node_limit is None else f"the first {node_limit} nodes"
     return {"value": nodes / wall, "unit": UNIT, "cores": len(chunks), "kind": "oracle",
-            "sample": f"{reqs_total} requests of the workload ({nodes} tree nodes, all query "
-                      f"heads, full step per request) over {len(chunks)} spawn workers, "
-                      f"{wall:.1f} s wall"}
+            "sample": f"{reqs_total} requests of the workload's first step ({what} of each, all query "
+                      f"heads: {nodes} tree nodes verified, full step per request) over "
+                      f"{len(chunks)} spawn workers, {wall:.1f} s wall"}
 
 
 def rank_seed(config, rank):
@@ -574,6 +591,11 @@ def reduce_over_ranks(times_ms, tokens, world, device):
     return [float(t) for t in mx.tolist()], float(sm[0])
 
 
+# oracle sample for the CPU baseline and the reference arm: config 5's
+# requests have prompts of 4K-32K tokens, so a few nodes of each
+ORACLE_NODE_LIMIT = {5: 4}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -581,8 +603,10 @@ def run_reference(args):
     from gen import workloads as wl
     w = wl.make_config(args.config)
     cores = os.cpu_count() or 1
-    # each step: one request's verification on the oracle; size so the run ends in minutes
-    n_first, t_first = _oracle_worker((w, [0], None))
+    # each step: one request's verification on the oracle (a bounded number of
+    # its nodes); sized so the whole run ends in minutes
+    cap = ORACLE_NODE_LIMIT.get(args.config)
+    n_first, t_first = _oracle_worker((w, [0], cap))
     budget = 150.0
     per_step = budget / max(1, args.steps + args.warmup)
     node_limit = max(1, int(n_first * min(1.0, per_step / max(t_first, 1e-6))))
@@ -602,7 +626,8 @@ def run_reference(args):
         "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step verifies {node_limit} node(s) (all query heads) "
-                                   f"of one request on the CPU oracle, single process"},
+                                   f"of one request of the workload's first step on the CPU "
+                                   f"oracle, single process"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "host_cores_available": cores,
     }
@@ -610,6 +635,173 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+def make_flush(dev):
+    import torch
+
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int32, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    class _Flush:
+        """Evict the L2 before a timed step: write a buffer larger than the
+        126 MB L2, then read another one so the lines left behind are clean
+        (otherwise the step would pay for writing the flush data back)."""
+
+        @staticmethod
+        def zero_():
+            flush_w.zero_()
+            flush_sink.add_(flush_r.sum())
+
+    return _Flush()
+
+
+def timed_replays(graphs, stream, flush, n):
+    """CUDA-event time (ms) of n replays cycling through ``graphs``, the L2
+    flushed (outside the events) before each."""
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush.zero_()
+        evs[i][0].record(stream)
+        graphs[i % len(graphs)].replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_of(nbytes, flops, attn_s, hbm_peak, tf_peak, src):
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
+    roof_s = max(nbytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
+    gbs = nbytes / attn_s / 1e9
+    tfs = flops / attn_s / 1e12
+    if flops / nbytes < ridge:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}
+    else:
+        roof = {"bound": "tensor", "achieved": tfs, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": tfs / tf_peak}
+    roof.update(peak_source=src, algorithmic_bytes=nbytes, algorithmic_flops=flops,
+                attention_us=attn_s * 1e6, roofline_us=roof_s * 1e6,
+                frac_of_roofline_time=roof_s / attn_s, frac_of_nominal_8tbs=gbs / 8000.0)
+    return roof
+
+
+def prepare_multistep(w0, dev, nsteps, seed):
+    """Run the config-5 loop once, untimed: verify -> accept + commit (block
+    release) -> host allocator (released blocks back on the free list, blocks
+    for the next tree's slots taken from it) -> next tree at P + 1 + a, with
+    fresh EAGLE-style trees. Returns per step (DeviceBatch, block-table
+    snapshot the step starts from, inputs); every step's batch shares one KV
+    pool, block table and workspace. A replay of the steps in order repeats
+    the same work: step k reads only prompt slots no later step writes."""
+    import torch
+
+    from gen import workloads as wl
+    from speculative_decoding_tree_build_gb300.step import DeviceBatch
+
+    rng = np.random.default_rng(seed)
+    out = []
+    w = w0
+    base = None
+    for k in range(nsteps):
+        db = DeviceBatch(w, device=dev) if base is None else DeviceBatch(w, device=dev, share=base)
+        base = base or db
+        snap = torch.from_numpy(np.concatenate([np.ascontiguousarray(w["block_table"], np.int32).reshape(-1),
+                                                np.asarray(w["n_blocks"], np.int32)])).to(dev)
+        db.table_state.copy_(snap)
+        db.status.zero_()
+        db.tree_build()
+        db.attention()
+        db.accept_commit()
+        torch.cuda.synchronize()
+        st = db.status.cpu().numpy()
+        if np.any(st != 0):
+            raise RuntimeError(f"multi-step workload: step {k} produced status flags {st}")
+        out.append((db, snap, w))
+        if k == nsteps - 1:
+            break
+        new_len = db.new_len.cpu().numpy()
+        bonus = db.bonus.cpu().numpy()
+        rel = db.released.cpu().numpy()
+        cnt = db.released_count.cpu().numpy()
+        tab = db.table_state.cpu().numpy()
+        nb = w["block_table"].size
+        free = list(w["free_blocks"])
+        for b in range(w["batch"]):
+            free.extend(int(x) for x in rel[b][:cnt[b]])
+        state = dict(w, block_table=tab[:nb].reshape(w["block_table"].shape).copy(),
+                     n_blocks=tab[nb:].copy(), free_blocks=free)
+        trees = []
+        for b in range(w["batch"]):
+            n_tree = int(rng.choice([16, 32, 64, 128]))
+            trees.append(wl.eagle_tree(rng, 0, int(rng.integers(4, 11)), n_tree, wl.VOCAB_LLAMA,
+                                       2.0, until_count=True)[:2])
+        w = wl.next_step_inputs(rng, state, new_len, bonus, trees)
+    return out
+
+
+def measure_single(cfg, dev, stream, flush, rank, iters, hbm_peak, tf_peak, src):
+    """One verification step of workload ``cfg``, replayed as one CUDA graph
+    from a restored block table; its attention call timed in its own loop."""
+    import torch
+
+    from gen import workloads as wl
+    from speculative_decoding_tree_build_gb300.step import DeviceBatch
+
+    w = wl.make_config(cfg, seed=rank_seed(cfg, rank))
+    db = DeviceBatch(w, device=dev)
+    table0 = db.table_state.clone()
+
+    def pre():
+        db.table_state.copy_(table0, non_blocking=True)   # allocator refill
+        db.tree_build()
+
+    def step():
+        pre()
+        db.attention()
+        db.accept_commit()
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            flush.zero_()
+            step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    if int(db.status.abs().sum()) != 0:
+        raise RuntimeError(f"config {cfg}: status flags")
+    depth = db.depth.cpu().numpy()
+    g_step, g_pre, g_attn = (torch.cuda.CUDAGraph() for _ in range(3))
+    with torch.cuda.graph(g_step, stream=side):
+        step()
+    with torch.cuda.graph(g_pre, stream=side):
+        pre()
+    with torch.cuda.graph(g_attn, stream=side):
+        db.attention()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        flush.zero_()
+        g_step.replay()
+    step_ms = float(np.mean(timed_replays([g_step], stream, flush, iters)))
+    g_pre.replay()
+    attn_ms = float(np.mean(timed_replays([g_attn], stream, flush, iters)))
+    if int(db.status.abs().sum()) != 0:
+        raise RuntimeError(f"config {cfg}: replay status flags")
+    tokens = int(w["cu_nodes"][-1])
+    nbytes, flops = attention_algorithmic(w, depth)
+    roof = roofline_of(nbytes, flops, attn_ms * 1e-3, hbm_peak, tf_peak, src)
+    roof["traffic"] = recorded_traffic(cfg)
+    return w, db, {"workload": workload_config(w)["workload"], "config": workload_config(w),
+                   "tokens_per_step": tokens, "ms_per_step": step_ms,
+                   "tokens_per_s": tokens / (step_ms * 1e-3),
+                   "attention_tokens_per_s": tokens / (attn_ms * 1e-3), "roofline": roof,
+                   "timing": f"{iters} flushed replays of the step's CUDA graph, and of the "
+                             f"attention call's, CUDA events"}
+
 
 def run_ours(args):
     import torch
@@ -626,193 +818,179 @@ def run_ours(args):
     from __graft_entry__ import build
     build()
     from gen import workloads as wl
-    from speculative_decoding_tree_build_gb300.step import DeviceBatch
 
-    w = wl.make_config(args.config, seed=rank_seed(args.config, rank))
-    db = DeviceBatch(w, device=dev)
+    hbm_peak, tf_peak, src = measured_peaks()
     stream = torch.cuda.current_stream(dev)
-    table0 = db.table_state.clone()          # block table + block counts, one buffer
-    tokens_per_step = int(w["cu_nodes"][-1])
-    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int32, device=dev)
-    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
-
-    class _Flush:
-        """Evict the L2 before a timed step: write a buffer larger than the
-        126 MB L2, then read another one so the lines left behind are clean
-        (otherwise the step would pay for writing the flush data back)."""
-
-        @staticmethod
-        def zero_():
-            flush_w.zero_()
-            flush_sink.add_(flush_r.sum())
-
-    flush = _Flush()
-
-    def pre():
-        db.table_state.copy_(table0, non_blocking=True)   # allocator refill
-        db.tree_build()
-
-    def post():
-        db.accept_commit()                   # greedy_accept + kv_commit, one kernel
-
-    def step():
-        pre()
-        db.attention()
-        post()
-
+    flush = make_flush(dev)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
+
+    if args.config != 5:
+        # a single-step workload as the headline
+        w, db, single = measure_single(args.config, dev, stream, flush, rank, args.steps,
+                                       hbm_peak, tf_peak, src)
+        multi = None
+    else:
+        w = wl.make_config(5, seed=rank_seed(5, rank))
+        multi = prepare_multistep(w, dev, MULTISTEP, seed=rank_seed(5, rank) + 77)
     side = torch.cuda.Stream(dev)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
+
+    if multi is not None:
+        # ---- the eight evolving steps, each its own CUDA graph: restore the
+        # step's block table (the allocator's result), tree_build, attention,
+        # accept + commit with block release; timed steps cycle through them
+        graphs, attn_graphs, pre_graphs = [], [], []
+        for db, snap, wk in multi:
+            def pre(db=db, snap=snap):
+                db.table_state.copy_(snap, non_blocking=True)
+                db.tree_build()
+
+            def step(db=db, pre=pre):
+                pre()
+                db.attention()
+                db.accept_commit()
+            side.wait_stream(stream)
+            g, ga, gp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                step()
+            with torch.cuda.graph(gp, stream=side):
+                pre()
+            with torch.cuda.graph(ga, stream=side):
+                db.attention()
+            graphs.append(g)
+            pre_graphs.append(gp)
+            attn_graphs.append(ga)
+        torch.cuda.synchronize()
         for _ in range(max(3, args.warmup)):
-            flush.zero_()
-            step()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    depth = db.depth.cpu().numpy()
-    st = db.status.cpu().numpy()
-    if np.any(st != 0):
-        raise RuntimeError(f"bench workload produced status flags {st}")
-
-    # The step's library calls are captured once into one CUDA graph (one graph
-    # per tree-size bucket is how a serving loop would run them) and replayed,
-    # so the timed region measures the GPU, not Python call overhead. The
-    # attention call alone is captured too, to time it in its own loop (an
-    # event between the step's grids would split the step into several graph
-    # launches, each with its own launch latency).
-    g_step, g_pre, g_attn = (torch.cuda.CUDAGraph() for _ in range(3))
-    with torch.cuda.graph(g_step, stream=side):
-        step()
-    with torch.cuda.graph(g_pre, stream=side):
-        pre()
-    with torch.cuda.graph(g_attn, stream=side):
-        db.attention()
-    torch.cuda.synchronize()
-    for _ in range(3):
-        flush.zero_()
-        g_step.replay()
-    torch.cuda.synchronize()
-    if int(db.status.abs().sum()) != 0:
-        raise RuntimeError("graph replay produced status flags")
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        g_step.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    # the attention call on its own: the block table as the step leaves it
-    # before the commit (refill + tree_build), then flushed replays
-    g_pre.replay()
-    for i in range(args.steps):
-        flush.zero_()
-        ev_a[i][0].record(stream)
-        g_attn.replay()
-        ev_a[i][1].record(stream)
-    torch.cuda.synchronize()
-    if int(db.status.abs().sum()) != 0:
-        raise RuntimeError("attention replay produced status flags")
-    clocks = sampler.stop() if sampler else None
-    step_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_a]))
-
-    # end to end through the public API: host inputs in, results out. The
-    # step's inputs (tree, tokens, raw q/k/v) sit in one device buffer and
-    # its results in another, so each direction is one copy per step.
-    h_in = db.inputs.cpu().pin_memory()
-    h_out = torch.empty_like(db.outputs, device="cpu").pin_memory()
-    h2d = h_in.numel() * h_in.element_size()
-    d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(3, args.e2e_steps)
-
-    def e2e_loop(run_step):
+            for g in graphs:
+                flush.zero_()
+                g.replay()
+        torch.cuda.synchronize()
+        tokens = [int(wk["cu_nodes"][-1]) for _, _, wk in multi]
+        if world > 1:
+            dist.barrier()
+        times = timed_replays(graphs, stream, flush, args.steps)
+        if world > 1:
+            dist.barrier()
+        step_ms = float(np.sum(times)) / args.steps
+        tokens_timed = float(sum(tokens[i % MULTISTEP] for i in range(args.steps)))
+        # each step's attention call in its own loop (table and tree of that step)
+        attn_ms, per_step = [], []
+        tot_b = tot_f = 0
+        for k, (db, snap, wk) in enumerate(multi):
+            pre_graphs[k].replay()
+            ms = float(np.mean(timed_replays([attn_graphs[k]], stream, flush, args.attn_iters)))
+            depth = db.depth.cpu().numpy()
+            nb, nf = attention_algorithmic(wk, depth)
+            attn_ms.append(ms)
+            tot_b += nb
+            tot_f += nf
+            per_step.append({"step": k, "tokens": tokens[k], "attention_us": ms * 1e3,
+                             "algorithmic_bytes": nb, "prompt_len_mean": float(np.mean(wk["prompt_len"])),
+                             "hbm_frac": nb / (ms * 1e-3) / 1e9 / hbm_peak})
+        for db, _, _ in multi:
+            if int(db.status.abs().sum()) != 0:
+                raise RuntimeError("multi-step replay produced status flags")
+        attn_total_s = float(np.sum(attn_ms)) * 1e-3
+        roof = roofline_of(tot_b, tot_f, attn_total_s, hbm_peak, tf_peak, src)
+        roof.update(traffic=recorded_traffic(5), per_step=per_step,
+                    attention_timing=("each step's attention call in its own loop of graph replays "
+                                      "on the step's stream, L2 flushed before each, CUDA events; "
+                                      "the eight steps' algorithmic bytes over the sum of their times"))
+        # end to end: each step's inputs copied in from pinned host memory (one
+        # copy), the step's graph, its results copied out (one copy)
+        h_in = [db.inputs.cpu().pin_memory() for db, _, _ in multi]
+        h_out = [torch.empty_like(db.outputs, device="cpu").pin_memory() for db, _, _ in multi]
+        n_e2e = max(MULTISTEP, args.e2e_steps)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(e2e_steps)]
-        for i in range(e2e_steps):
+               for _ in range(n_e2e)]
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            k = i % MULTISTEP
+            db = multi[k][0]
             flush.zero_()
             evs[i][0].record(stream)
-            db.inputs.copy_(h_in, non_blocking=True)
-            run_step()
-            h_out.copy_(db.outputs, non_blocking=True)
+            db.inputs.copy_(h_in[k], non_blocking=True)
+            graphs[k].replay()
+            h_out[k].copy_(db.outputs, non_blocking=True)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
-        if int(h_out[:4 * int(w["batch"])].view(torch.int32).abs().sum()) != 0:
-            raise RuntimeError("end-to-end step produced status flags")
-        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
-
-    def graph_step():
-        g_step.replay()
-
-    e2e_ms = e2e_loop(graph_step)          # host buffers in/out, graph-replayed API calls
-    e2e_eager_ms = e2e_loop(step)          # host buffers in/out, one Python call per API entry
-
-    (step_ms, attn_ms, e2e_ms), tokens_all = reduce_over_ranks(
-        [step_ms, attn_ms, e2e_ms], tokens_per_step, world, dev)
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
-
-    nbytes, flops = attention_algorithmic(w, depth)
-    hbm_peak, tf_peak, src = measured_peaks()
-    attn_gbs = nbytes / (attn_ms * 1e-3) / 1e9
-    attn_tfs = flops / (attn_ms * 1e-3) / 1e12
-    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
-    bound = "hbm" if flops / nbytes < ridge else "tensor"
-    roof_s = max(nbytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
-                "frac": attn_gbs / hbm_peak}
+        for k, (db, _, wk) in enumerate(multi):
+            if int(h_out[k][:4 * int(wk["batch"])].view(torch.int32).abs().sum()) != 0:
+                raise RuntimeError("end-to-end step produced status flags")
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        h2d = float(np.mean([t.numel() * t.element_size() for t in h_in]))
+        d2h = float(np.mean([t.numel() * t.element_size() for t in h_out]))
+        (step_ms, e2e_ms), tokens_all = reduce_over_ranks([step_ms, e2e_ms], tokens_timed / args.steps,
+                                                          world, dev)
+        headline_cfg = dict(workload_config(w), workload="llama3-8b-attn-ragged-eagle-8steps",
+                            steps_per_cycle=MULTISTEP,
+                            loop=("verify -> greedy accept + KV commit with block release -> host "
+                                  "allocator (released blocks back on the free list, the next tree's "
+                                  "slots allocated) -> next EAGLE-style tree at P + 1 + a; the eight "
+                                  "steps precomputed once, then replayed in order (each timed step "
+                                  "restores its step's block table, as the allocator leaves it)"),
+                            tokens_per_step=tokens,
+                            prompt_len_mean_per_step=[float(np.mean(wk["prompt_len"])) for _, _, wk in multi])
+        line = {
+            "metric": METRIC, "value": tokens_all / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": headline_cfg, "roofline": roof,
+            "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "mode": "pinned host inputs of each step copied in (one copy), results copied out "
+                            "(one copy), the step's library calls replayed from its CUDA graph"},
+            "gpu_launches": 5 * args.steps,   # tree_build, rope_append, attn_tc, attn_merge, accept_commit
+            "attention_tokens_per_s": float(sum(tokens)) / attn_total_s,
+        }
+        w0, db0 = multi[0][2], multi[0][0]
     else:
-        roof = {"bound": "tensor", "achieved": attn_tfs, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": attn_tfs / tf_peak}
-    roof.update(traffic=recorded_traffic(args.config), peak_source=src,
-                algorithmic_bytes=nbytes, algorithmic_flops=flops,
-                attention_us=attn_ms * 1e3, roofline_us=roof_s * 1e6,
-                attention_timing=("the attention call's own loop of graph replays on the step's "
-                                  "stream, L2 flushed before each, CUDA events"),
-                frac_of_roofline_time=roof_s / (attn_ms * 1e-3),
-                frac_of_nominal_8tbs=attn_gbs / 8000.0)
-    line = {
-        "metric": METRIC, "value": tokens_all / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(w), "roofline": roof,
-        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "mode": "pinned host inputs copied in (one copy), results copied out (one copy), library calls "
-                        "replayed from CUDA graphs",
-                "eager_value": tokens_all / (e2e_eager_ms * 1e-3),
-                "eager_ms_per_step": e2e_eager_ms},
-        "gpu_launches": 5 * args.steps,     # tree_build, rope_append, attn_tc, attn_merge, accept_commit
-        "attention_tokens_per_s": tokens_all / (attn_ms * 1e-3),
-        "clocks": clocks,
-    }
-    if args.sampling_steps > 0:
-        line["sampling"] = measure_sampling(w, dev, stream, flush, args.sampling_steps, hbm_peak)
-        line["rejection_acceptance"] = measure_rejection(w, dev, stream, flush,
-                                                         args.sampling_steps, hbm_peak)
-        line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps,
-                                                     hbm_peak)
-        line["eagle_selection"] = measure_eagle(dev, stream, flush, args.sampling_steps)
-        line["dense_mask_export"] = measure_dense_mask(w, db, stream, flush, args.sampling_steps,
-                                                       hbm_peak)
+        (step_ms,), tokens_all = reduce_over_ranks([single["ms_per_step"]], single["tokens_per_step"],
+                                                   world, dev)
+        line = {
+            "metric": METRIC, "value": tokens_all / (step_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": single["config"], "roofline": single["roofline"],
+            "gpu_launches": 5 * args.steps,
+            "attention_tokens_per_s": single["attention_tokens_per_s"],
+        }
+        w0, db0 = w, db
+
+    # ---- the other workloads, one verification step each
+    if not args.no_sub and rank == 0:
+        subs = {}
+        for cfg in SUB_CONFIGS:
+            if cfg == args.config:
+                continue
+            _, _, res = measure_single(cfg, dev, stream, flush, rank, args.sub_iters, hbm_peak, tf_peak,
+                                       src)
+            subs[f"config{cfg}"] = res
+        line["sub_workloads"] = subs
+    clocks = sampler.stop() if sampler else None
+    line["clocks"] = clocks
     if world > 1:
         dist.destroy_process_group()
+    if rank != 0:
+        return
+    if args.sampling_steps > 0:
+        # the NEXT-row kernels on the config-2 workload's trees (small rows)
+        w2 = wl.make_config(2, seed=rank_seed(2, rank))
+        from speculative_decoding_tree_build_gb300.step import DeviceBatch
+        db2 = DeviceBatch(w2, device=dev)
+        db2.tree_build()
+        torch.cuda.synchronize()
+        line["sampling"] = measure_sampling(w2, dev, stream, flush, args.sampling_steps, hbm_peak)
+        line["rejection_acceptance"] = measure_rejection(w2, dev, stream, flush, args.sampling_steps,
+                                                         hbm_peak)
+        line["ddtree_construction"] = measure_ddtree(dev, stream, flush, args.sampling_steps, hbm_peak)
+        line["eagle_selection"] = measure_eagle(dev, stream, flush, args.sampling_steps)
+        line["dense_mask_export"] = measure_dense_mask(w2, db2, stream, flush, args.sampling_steps,
+                                                       hbm_peak)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w0, args.cpu_seconds, ORACLE_NODE_LIMIT.get(args.config))
     print(json.dumps(line), flush=True)
 
 

@@ -27,8 +27,10 @@ generated one.
 
 from __future__ import annotations
 
+import concurrent.futures
 import heapq
 import math
+import os
 from dataclasses import dataclass
 
 import numpy as np
@@ -46,12 +48,28 @@ def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16(rng: np.random.Generator, shape, chunk=1 << 24) -> np.ndarray:
-    """bf16 bit patterns of N(0, 1) draws, generated in chunks to bound memory."""
+    """bf16 bit patterns of N(0, 1) draws, generated in chunks to bound memory.
+
+    Up to one chunk comes from ``rng`` itself. Larger arrays (the paged KV
+    pools) are split into chunks of their own seeded streams - chunk i draws
+    from a generator seeded with (one draw of ``rng``, i) - and generated on
+    several threads; the result depends only on ``rng``'s state, not on the
+    thread count."""
     total = int(np.prod(shape))
     out = np.empty(total, dtype=np.uint16)
-    for s in range(0, total, chunk):
-        e = min(total, s + chunk)
-        out[s:e] = bf16_bits_from_f32(rng.standard_normal(e - s, dtype=np.float32))
+    if total <= chunk:
+        out[:] = bf16_bits_from_f32(rng.standard_normal(total, dtype=np.float32))
+        return out.reshape(shape)
+    base = int(rng.integers(0, 2 ** 62))
+
+    def fill(i):
+        s, e = i * chunk, min(total, (i + 1) * chunk)
+        g = np.random.default_rng([base, i])
+        out[s:e] = bf16_bits_from_f32(g.standard_normal(e - s, dtype=np.float32))
+
+    n = -(-total // chunk)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1, n)) as ex:
+        list(ex.map(fill, range(n)))
     return out.reshape(shape)
 
 

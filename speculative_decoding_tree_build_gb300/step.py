@@ -39,7 +39,10 @@ class DeviceBatch:
     """A workload dict (see gen/workloads.py) resident on a CUDA device, plus the
     output buffers and the attention workspace."""
 
-    def __init__(self, w, device="cuda", workspace=None):
+    def __init__(self, w, device="cuda", workspace=None, share=None):
+        """``share``: another DeviceBatch of the same batch whose KV pools,
+        block table and workspace this one uses (the steps of a multi-step
+        run keep their own inputs and outputs over one cache)."""
         dev = torch.device(device)
         self.w = w
         self.device = dev
@@ -48,13 +51,18 @@ class DeviceBatch:
         self.max_nodes = int(w["max_nodes"])
         self.max_depth = int(w["max_depth"])
         self.batch = int(w["batch"])
-        self.k_cache = _bf16(w["k_cache"], dev)
-        self.v_cache = _bf16(w["v_cache"], dev)
-        # block table and per-request block counts share one buffer, so an
-        # allocator can save or restore both with one copy
         table = np.ascontiguousarray(w["block_table"], dtype=np.int32)
-        nblk = np.ascontiguousarray(w["n_blocks"], dtype=np.int32)
-        self.table_state = _i32(np.concatenate([table.reshape(-1), nblk]), dev)
+        if share is not None:
+            self.k_cache, self.v_cache = share.k_cache, share.v_cache
+            self.table_state = share.table_state
+            workspace = share.workspace if workspace is None else workspace
+        else:
+            self.k_cache = _bf16(w["k_cache"], dev)
+            self.v_cache = _bf16(w["v_cache"], dev)
+            # block table and per-request block counts share one buffer, so an
+            # allocator can save or restore both with one copy
+            nblk = np.ascontiguousarray(w["n_blocks"], dtype=np.int32)
+            self.table_state = _i32(np.concatenate([table.reshape(-1), nblk]), dev)
         self.block_table = self.table_state[:table.size].view(table.shape)
         self.n_blocks = self.table_state[table.size:]
         self.load_step_inputs(w)
