@@ -110,7 +110,15 @@ def tree_attention_verify_ref(q_rot, k_tree_rot, v_tree, parents, k_cache_bits,
     q_rot [N, Hq, D], k_tree_rot/v_tree [N, Hkv, D] are float64 (the rotated,
     bf16-rounded values); the prompt K/V are read from the paged pools.
     ``pairs`` optionally restricts the computed (node, q_head) outputs (the
-    others are NaN), for sampled checks at large sizes.
+    others are NaN), for checks of selected outputs at large sizes.
+
+    Same visible set and softmax as ``branch_attention_ref``: query (i, h)
+    attends to all P prompt keys of KV head g = h // G plus the keys of node
+    i's root-to-node chain. The scores against the prompt keys of one KV head
+    are taken for all its selected queries in one matrix product, and each
+    output is sum_j exp(s_j - m) v_j / sum_j exp(s_j - m) over those keys, m
+    the row's largest score (the softmax written out, normalised after the
+    weighted sum).
     """
     kp = gather_prompt_kv_ref(k_cache_bits, block_table_row, prompt_len, block_size)
     vp = gather_prompt_kv_ref(v_cache_bits, block_table_row, prompt_len, block_size)
@@ -122,11 +130,26 @@ def tree_attention_verify_ref(q_rot, k_tree_rot, v_tree, parents, k_cache_bits,
     if pairs is None:
         pairs = [(i, h) for i in range(n) for h in range(hq)]
     out = np.full((n, hq, d), np.nan, dtype=np.float64)
-    for i, h in pairs:
-        chain = ancestor_path(parents, i)
-        g = h // group
-        keys = np.concatenate([kp[:, g, :], k_tree_rot[chain, g, :]], axis=0)
-        vals = np.concatenate([vp[:, g, :], v_tree[chain, g, :]], axis=0)
-        p = _softmax((keys @ q_rot[i, h]) * scale)
-        out[i, h] = p @ vals
+    chains = {}
+    for g in range(hkv):
+        sel = [(i, h) for (i, h) in pairs if h // group == g]
+        if not sel:
+            continue
+        kg = np.ascontiguousarray(kp[:, g, :])                 # [P, D]
+        vg = np.ascontiguousarray(vp[:, g, :])
+        qs = np.stack([q_rot[i, h] for (i, h) in sel])         # [m, D]
+        s_prompt = (qs @ kg.T) * scale                         # [m, P]
+        s_chain = []
+        for r, (i, _) in enumerate(sel):
+            if i not in chains:
+                chains[i] = ancestor_path(parents, i)
+            s_chain.append((k_tree_rot[chains[i], g, :] @ qs[r]) * scale)
+        m = np.array([max(np.max(s_prompt[r], initial=-np.inf), np.max(s_chain[r]))
+                      for r in range(len(sel))])
+        e_prompt = np.exp(s_prompt - m[:, None])
+        num = e_prompt @ vg                                    # [m, D]
+        den = e_prompt.sum(axis=1)
+        for r, (i, h) in enumerate(sel):
+            e_chain = np.exp(s_chain[r] - m[r])
+            out[i, h] = (num[r] + e_chain @ v_tree[chains[i], g, :]) / (den[r] + e_chain.sum())
     return out

@@ -31,6 +31,43 @@ def sample_pairs(w, per_request, seed=0):
     return out
 
 
+def split_unit_pairs(w, grid, tile_keys=128):
+    """(node, q_head) pairs of every attention work unit whose key tiles the
+    kernel divides between CTAs.
+
+    The kernel's plan: a unit is one request, one KV head and up to
+    8 * (32 // G) consecutive nodes; it spans ceil((P + N) / tile_keys) key
+    tiles; units are ordered by request, KV head, node range, and the global
+    tile sequence is cut into ``grid`` near-equal contiguous ranges (the first
+    total % grid ranges one tile longer). A unit is split when a range
+    boundary falls strictly inside it; its partial results then go through
+    the merge. Returns (pairs per request, number of split units)."""
+    hq, hkv = w["num_q_heads"], w["num_kv_heads"]
+    g = hq // hkv
+    unit_nodes = 8 * (32 // g)
+    cu = w["cu_nodes"]
+    units, t = [], 0
+    for b in range(w["batch"]):
+        n = int(cu[b + 1] - cu[b])
+        tiles = -(-(int(w["prompt_len"][b]) + n) // tile_keys)
+        for kvh in range(hkv):
+            for rg in range(-(-n // unit_nodes)):
+                units.append((b, kvh, rg * unit_nodes, min(n, (rg + 1) * unit_nodes), t, t + tiles))
+                t += tiles
+    q, rem = divmod(t, grid)
+    bounds = np.array([c * q + min(c, rem) for c in range(1, grid)], dtype=np.int64)
+    out, n_split = {}, 0
+    for (b, kvh, i0, i1, u0, u1) in units:
+        if not np.any((bounds > u0) & (bounds < u1)):
+            continue
+        n_split += 1
+        pairs = out.setdefault(b, set())
+        for i in range(i0, i1):
+            for h in range(kvh * g, (kvh + 1) * g):
+                pairs.add((i, h))
+    return {b: sorted(v) for b, v in out.items()}, n_split
+
+
 def compare_out(gpu_out, ref_out, w, pairs=None):
     """Element-wise attention comparison on all (or the sampled) outputs."""
     cu = w["cu_nodes"]
@@ -146,6 +183,6 @@ def oracle_step(w, sample=None, commit=True):
     return verify_step_ref(w, sample=sample, commit=commit)
 
 
-__all__ = ["ATOL", "REL_FRO", "sample_pairs", "compare_out", "bf16_ulp_diff", "tentative_rows",
+__all__ = ["ATOL", "REL_FRO", "sample_pairs", "split_unit_pairs", "compare_out", "bf16_ulp_diff", "tentative_rows",
            "run_gpu", "rope_close", "check_tree_outputs", "check_accept_outputs", "oracle_step",
            "bf16_bits_to_f64"]

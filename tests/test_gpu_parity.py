@@ -15,7 +15,8 @@ from speculative_decoding_tree_build_gb300.build import build
 from speculative_decoding_tree_build_gb300.step import DeviceBatch
 
 from parity import (bf16_bits_to_f64, bf16_ulp_diff, check_accept_outputs, check_tree_outputs,
-                    compare_out, oracle_step, rope_close, run_gpu, sample_pairs, tentative_rows)
+                    compare_out, oracle_step, rope_close, run_gpu, sample_pairs, split_unit_pairs,
+                    tentative_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -105,9 +106,15 @@ def test_step_small_fused_accept_commit(cfg):
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_step_full_size_sampled(cfg):
     """Full workload sizes, in the bench's launch configuration; attention
-    checked on sampled (node, head) outputs, everything else exhaustively."""
+    checked on every (node, head) of each unit whose key range is split
+    between CTAs (merged partials) and on sampled outputs of the rest;
+    everything else exhaustively."""
     w = wl.make_config(cfg)
     pairs = sample_pairs(w, per_request=3, seed=cfg)
+    split, n_split = split_unit_pairs(w, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert n_split > 0
+    for b, extra in split.items():
+        pairs[b] = sorted(set(pairs.get(b, [])) | set(extra))
     _run_and_check(w, pairs)
 
 

@@ -12,7 +12,8 @@ from oracle import (
     ST_BAD_BLOCK, ST_BAD_PARENT, ST_BAD_ROOT, ST_BAD_SIZE, ST_OK, ST_PATH_OVERFLOW,
     bf16_bits_to_f64, branch_attention_ref, dense_tree_mask_ref, f64_to_bf16_bits,
     gather_prompt_kv_ref, greedy_accept_ref, kv_commit_ref, packed_attention_ref,
-    rope_inv_freq_f32, rope_ref, round_to_bf16, tree_build_ref, verify_branches_ref,
+    rope_inv_freq_f32, rope_ref, round_to_bf16, tree_attention_verify_ref, tree_build_ref,
+    verify_branches_ref,
 )
 
 # --------------------------------------------------------------------------
@@ -290,6 +291,37 @@ def test_attention_closed_forms():
             g = h // (hq // hkv)
             want = (vp[:, g].sum(0) + vt[chains[i], g].sum(0)) / (p + len(chains[i]))
             assert np.allclose(out[i, h], want, atol=1e-14)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_paged_step_attention_equals_branch_gather(seed):
+    """The step oracle's attention (prompt scores per KV head in one matrix
+    product, softmax normalised after the weighted sum) equals the per-node
+    gather on the same keys, for all outputs and for a selected subset; the
+    unselected outputs stay NaN. Covers an empty prompt and GQA groups."""
+    rng = np.random.default_rng(40 + seed)
+    bs, hq, hkv, d = 4, 8, 2, 16
+    n = int(rng.integers(1, 30))
+    plen = [0, 1, 17, 45][seed]
+    parents, _ = random_tree(rng, n)
+    nblk = -(-(plen + n) // bs) + 3
+    table = rng.permutation(nblk)[: -(-(plen + n) // bs)]
+    kpool = f64_to_bf16_bits(rng.standard_normal((nblk, hkv, bs, d)))
+    vpool = f64_to_bf16_bits(rng.standard_normal((nblk, hkv, bs, d)))
+    q = rng.standard_normal((n, hq, d)) * 2.0
+    kt, vt = rng.standard_normal((n, hkv, d)), rng.standard_normal((n, hkv, d))
+    kp = gather_prompt_kv_ref(kpool, table, plen, bs)
+    vp = gather_prompt_kv_ref(vpool, table, plen, bs)
+    want = branch_attention_ref(q, kp, vp, kt, vt, parents)
+    got = tree_attention_verify_ref(q, kt, vt, parents, kpool, vpool, table, plen, bs)
+    assert np.max(np.abs(got - want)) < 1e-13
+    pairs = sorted({(int(rng.integers(0, n)), int(rng.integers(0, hq))) for _ in range(7)})
+    part = tree_attention_verify_ref(q, kt, vt, parents, kpool, vpool, table, plen, bs, pairs=pairs)
+    sel = np.zeros((n, hq), bool)
+    for i, h in pairs:
+        sel[i, h] = True
+    assert np.max(np.abs(part[sel] - want[sel])) < 1e-13
+    assert np.all(np.isnan(part[~sel]))
 
 
 def test_paged_gather_follows_block_table():
