@@ -290,57 +290,146 @@ __device__ __forceinline__ TcShape tc_shape(const TcParams& p, int b) {
   return r;
 }
 
-// exclusive prefix of per-request tile counts (all threads call)
-__device__ void tc_plan_prefix(const TcParams& p, int* s_pre, int* s_tmp) {
+// Work plan. The tiles of all units form one global sequence (request,
+// KV head, row group, key tile), and each CTA takes a contiguous range of it.
+// The ranges are cut by estimated cost rather than by tile count: a 128-key
+// step of a two-tile unit costs more than one of a one-tile unit, and every
+// unit has a fixed cost (Q load, pipeline fill, epilogue). In cost units a
+// unit is laid out as [kCostUnit + w | w | w ...] (w per tile); tile k starts
+// at 0 for k = 0, else at kCostUnit + k * w; CTA c owns the tiles whose start
+// lies in [floor(c W / grid), floor((c + 1) W / grid)), W the total cost.
+constexpr int kCostTwo = 10;        // one step of a two-tile unit
+constexpr int kCostOne = 7;         // one step of a one-tile unit
+constexpr int kCostUnit = 21;       // fixed cost of a unit
+
+__device__ __forceinline__ int tc_mt(int nodes, int npq) { return (nodes + 4 * npq - 1) / (4 * npq); }
+
+__device__ __forceinline__ int tc_step_cost(int mt) { return mt == 2 ? kCostTwo : kCostOne; }
+
+// row group rg of a request: its M tiles
+__device__ __forceinline__ int tc_rg_mt(const TcShape& r, int rg, int npq) {
+  return tc_mt(min(tc_unit_nodes(npq), r.n - rg * tc_unit_nodes(npq)), npq);
+}
+
+__device__ __forceinline__ int tc_unit_cost(const TcShape& r, int rg, int npq) {
+  return kCostUnit + r.tiles * tc_step_cost(tc_rg_mt(r, rg, npq));
+}
+
+// cost of one KV head's units of a request (all row groups)
+__device__ __forceinline__ int tc_head_cost(const TcShape& r, int npq) {
+  if (r.nrg == 0) return 0;
+  return (r.nrg - 1) * tc_unit_cost(r, 0, npq) + tc_unit_cost(r, r.nrg - 1, npq);
+}
+
+// Exclusive prefixes of per-request tile counts (s_pre) and costs (sw_pre),
+// entry `batch` holding the totals (all threads call).
+__device__ void tc_plan_prefix(const TcParams& p, int* s_pre, int* sw_pre, int* s_tmp) {
   const int nt = blockDim.x, tid = threadIdx.x;
   const int per = (p.batch + nt - 1) / nt;
   const int lo = min(p.batch, tid * per), hi = min(p.batch, lo + per);
-  int sum = 0;
+  int sum = 0, wsum = 0;
   for (int b = lo; b < hi; ++b) {
     const TcShape r = tc_shape(p, b);
     sum += p.hkv * r.nrg * r.tiles;
+    wsum += p.hkv * tc_head_cost(r, p.npq);
   }
-  // block-wide exclusive scan of the per-thread sums (warp shuffles, then
+  // block-wide exclusive scans of the per-thread sums (warp shuffles, then
   // one warp scans the per-warp totals)
   const int lane = tid & 31, wid = tid >> 5, nw = (nt + 31) >> 5;
-  int x = sum;
+  int x = sum, xw = wsum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int yw = __shfl_up_sync(0xffffffffu, xw, o);
+    if (lane >= o) {
+      x += y;
+      xw += yw;
+    }
   }
-  if (lane == 31) s_tmp[wid] = x;
+  if (lane == 31) {
+    s_tmp[wid] = x;
+    s_tmp[16 + wid] = xw;
+  }
   __syncthreads();
   if (wid == 0) {
-    int w = lane < nw ? s_tmp[lane] : 0;
+    int v = lane < nw ? s_tmp[lane] : 0;
+    int vw = lane < nw ? s_tmp[16 + lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      const int yw = __shfl_up_sync(0xffffffffu, vw, o);
+      if (lane >= o) {
+        v += y;
+        vw += yw;
+      }
     }
-    if (lane < nw) s_tmp[32 + lane] = w;            // inclusive per-warp totals
-    if (lane == nw - 1) s_pre[p.batch] = w;
+    if (lane < nw) {                                  // inclusive per-warp totals
+      s_tmp[32 + lane] = v;
+      s_tmp[48 + lane] = vw;
+    }
+    if (lane == nw - 1) {
+      s_pre[p.batch] = v;
+      sw_pre[p.batch] = vw;
+    }
   }
   __syncthreads();
   int run = x - sum + (wid > 0 ? s_tmp[32 + wid - 1] : 0);
+  int wrun = xw - wsum + (wid > 0 ? s_tmp[48 + wid - 1] : 0);
   for (int b = lo; b < hi; ++b) {
     s_pre[b] = run;
+    sw_pre[b] = wrun;
     const TcShape r = tc_shape(p, b);
     run += p.hkv * r.nrg * r.tiles;
+    wrun += p.hkv * tc_head_cost(r, p.npq);
   }
   __syncthreads();
 }
 
-__device__ __forceinline__ long long tc_cta_start(long long total, int grid, int c) {
-  const long long q = total / grid, rem = total % grid;
-  return c * q + min(static_cast<long long>(c), rem);
+// last request whose prefix entry is <= x (requests without work share their
+// successor's entry, so they are passed over)
+__device__ __forceinline__ int tc_find_request(const int* pre, int batch, long long x) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
-__device__ __forceinline__ int tc_cta_of(long long total, int grid, long long t) {
-  const long long q = total / grid, rem = total % grid;
-  const long long big = rem * (q + 1);
-  if (t < big) return static_cast<int>(t / (q + 1));
-  return static_cast<int>(rem + (t - big) / q);
+// First global tile of CTA c: the first tile whose cost position is at least
+// floor(c W / grid) (the total tile count for c = grid).
+__device__ long long tc_cta_start(const TcParams& p, const int* s_pre, const int* sw_pre, int c) {
+  const long long W = sw_pre[p.batch];
+  if (c >= p.grid || W == 0) return s_pre[p.batch];
+  const long long x = W * c / p.grid;
+  const int b = tc_find_request(sw_pre, p.batch, x);
+  const TcShape r = tc_shape(p, b);
+  const int wk = tc_head_cost(r, p.npq);
+  const long long local = x - sw_pre[b];
+  const int kvh = static_cast<int>(local / wk);
+  int rem = static_cast<int>(local % wk), rg = 0;
+  for (; rg < r.nrg - 1; ++rg) {
+    const int wu = tc_unit_cost(r, rg, p.npq);
+    if (rem < wu) break;
+    rem -= wu;
+  }
+  const int w = tc_step_cost(tc_rg_mt(r, rg, p.npq));
+  const int k = rem <= 0 ? 0 : max(1, (rem - kCostUnit + w - 1) / w);   // may be r.tiles: the next unit's first
+  return s_pre[b] + static_cast<long long>(kvh * r.nrg + rg) * r.tiles + k;
+}
+
+// The CTA whose range holds global tile t.
+__device__ int tc_cta_of(const TcParams& p, const int* s_pre, const int* sw_pre, long long t) {
+  const long long W = sw_pre[p.batch];
+  const int b = tc_find_request(s_pre, p.batch, t);
+  const TcShape r = tc_shape(p, b);
+  const long long local = t - s_pre[b];
+  const int unit = static_cast<int>(local / r.tiles), k = static_cast<int>(local % r.tiles);
+  const int kvh = unit / r.nrg, rg = unit % r.nrg;
+  const long long pos = sw_pre[b] + static_cast<long long>(kvh) * tc_head_cost(r, p.npq) +
+                        static_cast<long long>(rg) * tc_unit_cost(r, 0, p.npq) +
+                        (k == 0 ? 0 : kCostUnit + static_cast<long long>(k) * tc_step_cost(tc_rg_mt(r, rg, p.npq)));
+  return static_cast<int>(min(static_cast<long long>(p.grid - 1), ((pos + 1) * p.grid - 1) / W));
 }
 
 // Segment of this CTA's tile range that starts at global tile t. Without
@@ -499,8 +588,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint8_t* sK = smem + C::kQBytes;
   uint8_t* sV = sK + kStages * C::kStageBytes;
   int* s_pre = reinterpret_cast<int*>(sV + kStages * C::kStageBytes);
+  int* sw_pre = s_pre + p.batch + 1;
   __shared__ TcBars bars;
-  __shared__ int s_tmp[kTcThreads];
+  __shared__ int s_tmp[64];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ TcSeg s_last;                // the last segment of this CTA's range (merge task)
@@ -538,11 +628,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
-  tc_plan_prefix(p, s_pre, s_tmp);        // contains __syncthreads; reads only call inputs
+  tc_plan_prefix(p, s_pre, sw_pre, s_tmp);   // contains __syncthreads; reads only call inputs
   tc_fence_after();
-  const long long total = s_pre[p.batch];
-  const long long cs = tc_cta_start(total, p.grid, blockIdx.x);
-  const long long ce = tc_cta_start(total, p.grid, blockIdx.x + 1);
+  const long long cs = tc_cta_start(p, s_pre, sw_pre, blockIdx.x);
+  const long long ce = tc_cta_start(p, s_pre, sw_pre, blockIdx.x + 1);
+  if (cs == ce && threadIdx.x < 256) {
+    // A CTA without tiles may still lie between the contributors of a unit
+    // split across CTAs; its first partial slot, which the merge reads, then
+    // holds no keys (m = -inf, l = 0).
+    float* ml = reinterpret_cast<float*>(p.partials + static_cast<size_t>(2 * blockIdx.x) * kSlotBytes(D) +
+                                         static_cast<size_t>(256) * 2 * D);
+    ml[threadIdx.x] = -INFINITY;
+    ml[256 + threadIdx.x] = 0.f;
+  }
   const int G = p.group, npq = p.npq;
   const int32_t* table_base = p.block_table;
   if (warp == 2) {
@@ -997,7 +1095,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       rec[5] = last.t0;
       rec[6] = last.n;
       rec[7] = blockIdx.x;                                              // first contributor
-      rec[8] = tc_cta_of(total, p.grid, last.unit_t0 + last.ntiles - 1); // last contributor
+      rec[8] = tc_cta_of(p, s_pre, sw_pre, last.unit_t0 + last.ntiles - 1);   // last contributor
       rec[9] = last.my_slot;                                            // its slot
       rec[10] = last.nodes;
     }
@@ -1288,7 +1386,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   const int dev = current_device();
   if (dev < 0) return TV_ERR_CUDA;
   const size_t smem_fixed = (D == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem) + 1024;
-  const size_t smem = smem_fixed + static_cast<size_t>(batch + 1) * sizeof(int);
+  const size_t smem = smem_fixed + static_cast<size_t>(batch + 1) * 2 * sizeof(int);
   if (smem > 227 * 1024) return TV_ERR_BAD_SIZE;
 
   // The attention and merge grids are launched with programmatic stream

@@ -31,34 +31,58 @@ def sample_pairs(w, per_request, seed=0):
     return out
 
 
-def split_unit_pairs(w, grid, tile_keys=128):
-    """(node, q_head) pairs of every attention work unit whose key tiles the
-    kernel divides between CTAs.
+COST_TWO, COST_ONE, COST_UNIT = 10, 7, 21   # the kernel's step and unit costs
 
-    The kernel's plan: a unit is one request, one KV head and up to
-    8 * (32 // G) consecutive nodes; it spans ceil((P + N) / tile_keys) key
-    tiles; units are ordered by request, KV head, node range, and the global
-    tile sequence is cut into ``grid`` near-equal contiguous ranges (the first
-    total % grid ranges one tile longer). A unit is split when a range
-    boundary falls strictly inside it; its partial results then go through
-    the merge. Returns (pairs per request, number of split units)."""
+
+def attention_plan(w, grid, tile_keys=128):
+    """The attention kernel's work plan, restated on the host.
+
+    A unit is one request, one KV head and up to 8 * (32 // G) consecutive
+    nodes (one or two M tiles of 32 // G nodes per 32-row quarter); it spans
+    ceil((P + N) / tile_keys) key tiles. Units are ordered by request, KV
+    head, node range, giving one global tile sequence. In cost units a unit is
+    [COST_UNIT + c | c | c ...], c = COST_TWO or COST_ONE per tile by its M
+    tiles; tile k starts at 0 (k = 0) or COST_UNIT + k c, and CTA j owns the
+    tiles whose start lies in [floor(j W / grid), floor((j + 1) W / grid)).
+    Returns (units, starts): units as (request, kv head, first node, end node,
+    first global tile, end global tile, tile cost); starts[j] the first global
+    tile of CTA j (starts[grid] = total tiles)."""
     hq, hkv = w["num_q_heads"], w["num_kv_heads"]
     g = hq // hkv
-    unit_nodes = 8 * (32 // g)
+    npq = 32 // g
+    unit_nodes = 8 * npq
     cu = w["cu_nodes"]
-    units, t = [], 0
+    units, tile_pos = [], []          # tile_pos: cost position of every tile
+    t = pos = 0
     for b in range(w["batch"]):
         n = int(cu[b + 1] - cu[b])
         tiles = -(-(int(w["prompt_len"][b]) + n) // tile_keys)
         for kvh in range(hkv):
             for rg in range(-(-n // unit_nodes)):
-                units.append((b, kvh, rg * unit_nodes, min(n, (rg + 1) * unit_nodes), t, t + tiles))
+                i0, i1 = rg * unit_nodes, min(n, (rg + 1) * unit_nodes)
+                c = COST_TWO if -(-(i1 - i0) // (4 * npq)) == 2 else COST_ONE
+                units.append((b, kvh, i0, i1, t, t + tiles, c))
+                tile_pos.extend([pos] + [pos + COST_UNIT + k * c for k in range(1, tiles)])
                 t += tiles
-    q, rem = divmod(t, grid)
-    bounds = np.array([c * q + min(c, rem) for c in range(1, grid)], dtype=np.int64)
+                pos += COST_UNIT + tiles * c
+    bounds = [j * pos // grid for j in range(grid)] + [None]
+    tile_pos = np.asarray(tile_pos, dtype=np.int64)
+    starts = [int(np.searchsorted(tile_pos, bnd, side="left")) if bnd is not None else t for bnd in bounds]
+    return units, starts
+
+
+def split_unit_pairs(w, grid, tile_keys=128):
+    """(node, q_head) pairs of every attention work unit whose key tiles the
+    kernel divides between CTAs (``attention_plan``): a unit is split when a
+    CTA's first tile lies strictly inside it; its partial results then go
+    through the merge. Returns (pairs per request, number of split units)."""
+    hq, hkv = w["num_q_heads"], w["num_kv_heads"]
+    g = hq // hkv
+    units, starts = attention_plan(w, grid, tile_keys)
+    inner = np.asarray(starts[1:-1], dtype=np.int64)
     out, n_split = {}, 0
-    for (b, kvh, i0, i1, u0, u1) in units:
-        if not np.any((bounds > u0) & (bounds < u1)):
+    for (b, kvh, i0, i1, u0, u1, _) in units:
+        if not np.any((inner > u0) & (inner < u1)):
             continue
         n_split += 1
         pairs = out.setdefault(b, set())
@@ -183,6 +207,6 @@ def oracle_step(w, sample=None, commit=True):
     return verify_step_ref(w, sample=sample, commit=commit)
 
 
-__all__ = ["ATOL", "REL_FRO", "sample_pairs", "split_unit_pairs", "compare_out", "bf16_ulp_diff", "tentative_rows",
+__all__ = ["ATOL", "REL_FRO", "sample_pairs", "split_unit_pairs", "attention_plan", "compare_out", "bf16_ulp_diff", "tentative_rows",
            "run_gpu", "rope_close", "check_tree_outputs", "check_accept_outputs", "oracle_step",
            "bf16_bits_to_f64"]
