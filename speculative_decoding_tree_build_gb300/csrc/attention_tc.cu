@@ -57,8 +57,9 @@ constexpr int kTcBN = 128;          // keys per work-plan tile = per pipeline st
 constexpr int kTcThreads = 384;     // 12 warps
 constexpr int kTcMaxBatch = 4096;
 constexpr int kRopeNodes = 1;       // nodes per pre-pass CTA
-constexpr int kRopeBatch = 4;       // loads in flight per pre-pass thread
+constexpr int kRopeBatch = 3;       // loads in flight per pre-pass thread
 constexpr int kRopeThreads = 256;
+constexpr int kRopeMinBlocks = 8;   // 32 registers a thread: the whole SM's threads may run the pre-pass
 constexpr int kTaskInts = 16;       // merge-task record per attention CTA
 
 // bytes of one partial-result slot: O / l as fp16 [D/8 column blocks][256
@@ -101,14 +102,17 @@ struct RopeParams {
 
 // ------------------------------------------------------------ pre-pass
 
-template <int D>
-__global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_constant__ RopeParams p) {
+template <int D, bool kStyle0>
+__global__ void __launch_bounds__(kRopeThreads, kRopeMinBlocks) rope_append_kernel(const __grid_constant__ RopeParams p) {
   constexpr int D2 = D / 2;
   __shared__ float2 s_cs[kRopeNodes][D2];
   __shared__ int s_blk[kRopeNodes];      // cache block of each node's tentative slot
   grid_dependency_wait();                // inputs written by the previous kernel are visible
   grid_launch_dependents();              // the attention grid may start its prologue
-  const int b = blockIdx.y;
+  // blockIdx.x = request, blockIdx.y = node chunk: the CTAs are dispatched
+  // chunk by chunk, so those past a short tree's last node (which return at
+  // once) come after every request's first nodes
+  const int b = blockIdx.x;
   // the request's scalars, loaded together (one memory round trip)
   const int t0 = p.cu_nodes[b];
   const int t1 = p.cu_nodes[b + 1];
@@ -118,14 +122,14 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
   const int n = t1 - t0;
   if (n < 1 || n > p.max_nodes || plen < 0) return;             // tree_build flagged it
   if (static_cast<long long>(t0) + n > p.t_cap || t0 < 0) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_SIZE);
+    if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_SIZE);
     return;
   }
   if (st & TV_TREE_FLAGS) return;
-  const int i0 = blockIdx.x * kRopeNodes;
+  const int i0 = blockIdx.y * kRopeNodes;
   if (i0 >= n) return;
   const int i1 = min(n, i0 + kRopeNodes);
-  const bool style0 = p.rope_style == 0;
+  constexpr bool style0 = kStyle0;
   // Work item = one 16-byte vector (8 bf16) of one head of one node; style 0
   // rotates the pairs inside the vector, style 1 pairs vector v with vector
   // v + D/16. A thread loads kRopeBatch items before storing any, and the
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const __grid_
     s_cs[nd][pr] = make_float2(cs, sn);
   }
   if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
+    if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
     return;
   }
   for (int base = threadIdx.x; base < total; base += kRopeBatch * blockDim.x) {
@@ -1381,7 +1385,7 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   mp.group = group;
   mp.ntask = grid;
 
-  const dim3 rgrid((max_nodes + kRopeNodes - 1) / kRopeNodes, batch);
+  const dim3 rgrid(batch, (max_nodes + kRopeNodes - 1) / kRopeNodes);
   static size_t smem_set128[kMaxDevices] = {0}, smem_set64[kMaxDevices] = {0};
   const int dev = current_device();
   if (dev < 0) return TV_ERR_CUDA;
@@ -1424,12 +1428,14 @@ int launch_attention_tc(const tv_geom* geom, int batch, int max_nodes, const voi
   cudaError_t err;
   if (D == 128) {
     if (!ensure_smem(attn_tc_kernel<128>, smem, smem_set128, dev)) return TV_ERR_CUDA;
-    err = launch_pdl(rope_append_kernel<128>, rgrid, dim3(kRopeThreads), 0, stream, rp);
+    err = rp.rope_style == 0 ? launch_pdl(rope_append_kernel<128, true>, rgrid, dim3(kRopeThreads), 0, stream, rp)
+                             : launch_pdl(rope_append_kernel<128, false>, rgrid, dim3(kRopeThreads), 0, stream, rp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<128>, tp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&mcfg, attn_merge_kernel<128>, mp);
   } else {
     if (!ensure_smem(attn_tc_kernel<64>, smem, smem_set64, dev)) return TV_ERR_CUDA;
-    err = launch_pdl(rope_append_kernel<64>, rgrid, dim3(kRopeThreads), 0, stream, rp);
+    err = rp.rope_style == 0 ? launch_pdl(rope_append_kernel<64, true>, rgrid, dim3(kRopeThreads), 0, stream, rp)
+                             : launch_pdl(rope_append_kernel<64, false>, rgrid, dim3(kRopeThreads), 0, stream, rp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&acfg, attn_tc_kernel<64>, tp);
     if (err == cudaSuccess) err = cudaLaunchKernelEx(&mcfg, attn_merge_kernel<64>, mp);
   }
