@@ -705,17 +705,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(&bars.q_empty, (qs & 1) ^ 1, abort) : false, 0);
         if (!ok) break;
         ++qs;
-        if (lane == 0) {
-          // one box of npq nodes x G heads (<= 32 rows) per quarter and half;
-          // quarters without nodes are not loaded
-          const RowSplit rs = row_split(g.nodes, g.mt);
-          const uint32_t qbox = 64u * 2u * G * npq;
-          const int nq = min(4 * g.mt, g.nodes);
-          mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * nq);
-          for (int j = 0; j < nq; ++j)
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(sQ + ((j >> 2) * C::kHalves + h) * C::kQHalfBytes + (j & 3) * 4096, &p.qmap,
-                          h * 64, 0, g.kvh, g.t0 + g.node0 + quarter_first(rs, j), &bars.q_full);
+        // one box of npq nodes x G heads (<= 32 rows) per quarter and half,
+        // lane l issuing box l (quarter l / halves, half l % halves);
+        // quarters without nodes are not loaded
+        const RowSplit rs = row_split(g.nodes, g.mt);
+        const uint32_t qbox = 64u * 2u * G * npq;
+        const int nq = min(4 * g.mt, g.nodes);
+        if (lane == 0) mbar_arrive_expect_tx(&bars.q_full, qbox * C::kHalves * nq);
+        __syncwarp();
+        if (lane < nq * C::kHalves) {
+          const int j = lane / C::kHalves, h = lane % C::kHalves;
+          tma_load_4d(sQ + ((j >> 2) * C::kHalves + h) * C::kQHalfBytes + (j & 3) * 4096, &p.qmap,
+                      h * 64, 0, g.kvh, g.t0 + g.node0 + quarter_first(rs, j), &bars.q_full);
         }
       }
       const int32_t* trow = table_base + static_cast<size_t>(g.b) * p.max_blocks;
