@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import multiprocessing as mp
@@ -418,11 +419,20 @@ def measure_rejection(w, dev, stream, flush, iters, hbm_peak):
         "requests_per_s": bsz / (us * 1e-6)}
 
 
+def _code_only(text):
+    """Source text without comments and blank lines, so that a comment edit
+    does not disown the counters taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def source_sha(files):
+    """Hash of the code (comments stripped) of the given csrc files."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "speculative_decoding_tree_build_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -37,9 +37,10 @@
 //     major, spread evenly over the eight 32-row quarters of the two M tiles,
 //     so one K/V tile feeds up to 256 rows. Work plan: a unit is (request,
 //     KV head, group of up to 256 rows); all units' key tiles are laid end to
-//     end and every CTA takes an equal contiguous share, computed on the
-//     device from cu_nodes/prompt_len (no host round trip), so each CTA moves
-//     the same amount of KV whatever the prompt-length mix.
+//     end and every CTA takes a contiguous share of equal estimated cost
+//     (two-tile steps, one-tile steps and a fixed cost per unit weighted as
+//     measured), computed on the device from cu_nodes/prompt_len (no host
+//     round trip), so the CTAs finish together whatever the mix.
 //  3. attn_merge_kernel: a unit cut between CTAs left one partial per CTA;
 //     this grid merges them (log-sum-exp), many CTAs and loads in flight.
 //  Launches 2 and 3 use programmatic dependent launch so their prologues
