@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kRopeThreads, kRopeMinBlocks) rope_append_kern
   constexpr bool style0 = kStyle0;
   // Work item = one 16-byte vector (8 bf16) of one head of one node; style 0
   // rotates the pairs inside the vector, style 1 pairs vector v with vector
-  // v + D/16. A thread loads kRopeBatch items before storing any, and the
+  // v + D/16. A thread loads kBatch items before storing any, and the
   // first batch (every item, for the 8B geometry) is loaded before the
   // block-table check, so the CTA waits on memory about twice, not five times.
   constexpr int VPH = D / 8;
@@ -152,10 +152,13 @@ __global__ void __launch_bounds__(kRopeThreads, kRopeMinBlocks) rope_append_kern
       return reinterpret_cast<const uint4*>(p.k_new + (static_cast<size_t>(t) * p.hkv + h - p.hq) * D);
     return reinterpret_cast<const uint4*>(p.v_new + (static_cast<size_t>(t) * p.hkv + h - p.hq - p.hkv) * D);
   };
-  uint4 xa[kRopeBatch], xb[kRopeBatch];
+  // style 1 holds two vectors per item, so it keeps fewer items in flight
+  // within the 32-register budget
+  constexpr int kBatch = kStyle0 ? kRopeBatch : 1;
+  uint4 xa[kBatch], xb[kBatch];
   auto load_batch = [&](int base) {
 #pragma unroll
-    for (int u = 0; u < kRopeBatch; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       const int idx = base + u * blockDim.x;
       if (idx < total) {
         int nd, h, v;
@@ -190,10 +193,10 @@ __global__ void __launch_bounds__(kRopeThreads, kRopeMinBlocks) rope_append_kern
     if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.status + b, TV_ST_BAD_BLOCK);
     return;
   }
-  for (int base = threadIdx.x; base < total; base += kRopeBatch * blockDim.x) {
+  for (int base = threadIdx.x; base < total; base += kBatch * blockDim.x) {
     if (base != static_cast<int>(threadIdx.x)) load_batch(base);
 #pragma unroll
-    for (int u = 0; u < kRopeBatch; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       const int idx = base + u * blockDim.x;
       if (idx >= total) break;
       int nd, h, v;
