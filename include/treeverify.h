@@ -207,8 +207,8 @@ int tv_tree_attention_verify(const tv_geom* geom, int32_t batch, int32_t max_nod
                              size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
- * Allocation-free variant of tv_tree_attention_verify. The paper has no
- * counterpart to this call: it exists for callers that cannot obtain device
+ * Allocation-free variant of tv_tree_attention_verify. The published tree
+ * verification methods have no counterpart to this call: it exists for callers that cannot obtain device
  * memory - a plugin inside a host framework that only receives a stream and
  * tensors, code running while another component owns the whole device memory
  * pool, or a latency-critical loop that must not call cudaMalloc (which can

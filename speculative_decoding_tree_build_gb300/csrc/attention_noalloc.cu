@@ -12,7 +12,8 @@
 // The array is TV_NOALLOC_SCRATCH_BYTES (64 MiB) per GPU. It belongs to this
 // translation unit's module, which the CUDA runtime loads (and so reserves the
 // array) the first time the entry point is used on a device; it stays reserved
-// until the process exits. The paper has no counterpart to this call.
+// until the process exits. The published tree verification methods have no
+// counterpart to this call.
 #include "tv_common.cuh"
 
 namespace tv {
